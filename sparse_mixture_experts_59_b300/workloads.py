@@ -1,0 +1,162 @@
+"""Seeded synthetic inputs for the MoE layer workloads.
+
+This module is shared by the CUDA path's tests/bench and by the CPU oracle.  It
+draws random numbers and lays out tensors; it holds none of the method's
+arithmetic (no routing, no expert maths).
+
+Weight layout is the nn.Linear one used by the pages' listings:
+  Wr [E, d]      router ("gate") weight, no bias
+  W1 [E, F, d]   SwiGLU gate projection, or the GELU MLP's first Linear
+  W3 [E, F, d]   SwiGLU up projection (None for GELU)
+  W2 [E, d, F]   down projection / second Linear
+  b1 [E, F], b2 [E, d]   GELU MLP biases (None for SwiGLU)
+  S1, S3 [F_sh, d], S2 [d, F_sh]   shared SwiGLU expert (fine-grained workload)
+  logit_bias [E] fp32    fixed per-expert router-logit offset (skewed workload)
+
+Workloads (sizes from the pages' Mixtral / DeepSeek-V3 / Switch descriptions):
+  tiny_fp32        T=64  d=128  E=8   k=2 GELU(erf)+biases, cf 1.25, fp32
+  mixtral_prefill  T=4096 d=4096 F=14336 E=8 k=2 SwiGLU, dropless, bf16
+  mixtral_decode   same weights, T=32
+  fine_grained     T=8192 d=7168 F=2048 E=256 k=8 SwiGLU + shared F=2048, bf16
+  switch_skewed    T=16384 d=2048 F=8192 E=64 k=1 GELU+biases, cf 1.0, bf16,
+                   logit bias b_e = 1.5*ln(1/(e+1)^1.2)
+"""
+import math
+
+import torch
+
+WORKLOADS = {
+    "tiny_fp32": dict(T=64, d=128, F=256, E=8, k=2, act="gelu", has_bias=True,
+                      dtype="f32", capacity_factor=1.25, F_shared=0, seed=1000,
+                      init="uniform", router_scale=4.0, router_init="uniform", skew=False),
+    "mixtral_prefill": dict(T=4096, d=4096, F=14336, E=8, k=2, act="swiglu", has_bias=False,
+                            dtype="bf16", capacity_factor=0.0, F_shared=0, seed=1001,
+                            init="normal", router_scale=1.0, router_init="normal", skew=False),
+    "mixtral_decode": dict(T=32, d=4096, F=14336, E=8, k=2, act="swiglu", has_bias=False,
+                           dtype="bf16", capacity_factor=0.0, F_shared=0, seed=1002,
+                           weight_seed=1001, init="normal", router_scale=1.0,
+                           router_init="normal", skew=False),
+    "fine_grained": dict(T=8192, d=7168, F=2048, E=256, k=8, act="swiglu", has_bias=False,
+                         dtype="bf16", capacity_factor=0.0, F_shared=2048, seed=1003,
+                         init="normal", router_scale=1.0, router_init="normal", skew=False),
+    "switch_skewed": dict(T=16384, d=2048, F=8192, E=64, k=1, act="gelu", has_bias=True,
+                          dtype="bf16", capacity_factor=1.0, F_shared=0, seed=1004,
+                          init="uniform", router_scale=1.0, router_init="normal", skew=True),
+}
+
+_TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+def config(name: str, **overrides) -> dict:
+    """The named workload's configuration, with optional size overrides (the
+    parity tests use scaled-down copies that keep the structure)."""
+    cfg = dict(WORKLOADS[name])
+    cfg.update(overrides)
+    cfg["name"] = name
+    return cfg
+
+
+def skew_bias(E: int) -> torch.Tensor:
+    """Fixed per-expert logit offset b_e = 1.5*ln(1/rank_e^1.2), rank_e = e+1
+    (expert 0 is the hottest), giving a Zipf-like load."""
+    return torch.tensor([1.5 * math.log(1.0 / (e + 1) ** 1.2) for e in range(E)],
+                        dtype=torch.float32)
+
+
+def _gen(seed: int, device) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def _normal(shape, std, g, device, dtype, chunk_rows=None):
+    """N(0, std^2) drawn in fp32 and rounded once to `dtype`; drawn in chunks
+    along dim 0 to bound the fp32 temporary."""
+    out = torch.empty(shape, dtype=dtype, device=device)
+    n0 = shape[0]
+    step = chunk_rows or n0
+    for i in range(0, n0, step):
+        sl = out[i:i + step]
+        tmp = torch.randn(sl.shape, generator=g, device=device, dtype=torch.float32)
+        sl.copy_(tmp.mul_(std))
+    return out
+
+
+def _uniform(shape, bound, g, device, dtype, chunk_rows=None):
+    out = torch.empty(shape, dtype=dtype, device=device)
+    n0 = shape[0]
+    step = chunk_rows or n0
+    for i in range(0, n0, step):
+        sl = out[i:i + step]
+        tmp = torch.rand(sl.shape, generator=g, device=device, dtype=torch.float32)
+        sl.copy_(tmp.mul_(2.0 * bound).sub_(bound))
+    return out
+
+
+def make_weights(cfg: dict, device="cpu") -> dict:
+    """Expert, router and shared-expert weights for `cfg`, seeded by
+    cfg['weight_seed'] (default cfg['seed'])."""
+    d, F, E = cfg["d"], cfg["F"], cfg["E"]
+    dt = _TORCH_DTYPE[cfg["dtype"]]
+    g = _gen(cfg.get("weight_seed", cfg["seed"]) * 7919 + 17, device)
+    w = {}
+    # router
+    if cfg["router_init"] == "uniform":
+        w["Wr"] = _uniform((E, d), 1.0 / math.sqrt(d), g, device, torch.float32)
+    else:
+        w["Wr"] = _normal((E, d), 1.0 / math.sqrt(d), g, device, torch.float32)
+    if cfg.get("router_scale", 1.0) != 1.0:
+        w["Wr"].mul_(cfg["router_scale"])
+    w["Wr"] = w["Wr"].to(dt)
+    # experts
+    if cfg["init"] == "uniform":   # nn.Linear default: U(+-1/sqrt(fan_in))
+        w["W1"] = _uniform((E, F, d), 1.0 / math.sqrt(d), g, device, dt, 1)
+        w["W2"] = _uniform((E, d, F), 1.0 / math.sqrt(F), g, device, dt, 1)
+        w["W3"] = (_uniform((E, F, d), 1.0 / math.sqrt(d), g, device, dt, 1)
+                   if cfg["act"] == "swiglu" else None)
+        if cfg["has_bias"]:
+            w["b1"] = _uniform((E, F), 1.0 / math.sqrt(d), g, device, dt)
+            w["b2"] = _uniform((E, d), 1.0 / math.sqrt(F), g, device, dt)
+    else:
+        w["W1"] = _normal((E, F, d), 0.02, g, device, dt, 1)
+        w["W3"] = _normal((E, F, d), 0.02, g, device, dt, 1) if cfg["act"] == "swiglu" else None
+        w["W2"] = _normal((E, d, F), 0.02, g, device, dt, 1)
+        if cfg["has_bias"]:
+            w["b1"] = _normal((E, F), 0.02, g, device, dt)
+            w["b2"] = _normal((E, d), 0.02, g, device, dt)
+    if not cfg["has_bias"]:
+        w["b1"] = None
+        w["b2"] = None
+    Fs = cfg.get("F_shared", 0)
+    if Fs:
+        w["S1"] = _normal((Fs, d), 0.02, g, device, dt)
+        w["S3"] = _normal((Fs, d), 0.02, g, device, dt)
+        w["S2"] = _normal((d, Fs), 0.02, g, device, dt)
+    else:
+        w["S1"] = w["S3"] = w["S2"] = None
+    w["logit_bias"] = skew_bias(E).to(device) if cfg.get("skew") else None
+    return w
+
+
+def make_x(cfg: dict, device="cpu") -> torch.Tensor:
+    """Token activations x ~ N(0, 1) [T, d], seeded by cfg['seed']."""
+    g = _gen(cfg["seed"], device)
+    return _normal((cfg["T"], cfg["d"]), 1.0, g, device, _TORCH_DTYPE[cfg["dtype"]])
+
+
+def make_inputs(name_or_cfg, device="cpu", **overrides) -> dict:
+    """All inputs of one workload as a dict: cfg, x, Wr, logit_bias, W1, W3,
+    W2, b1, b2, S1, S3, S2."""
+    cfg = config(name_or_cfg, **overrides) if isinstance(name_or_cfg, str) else dict(name_or_cfg)
+    inp = make_weights(cfg, device)
+    inp["x"] = make_x(cfg, device)
+    inp["cfg"] = cfg
+    return inp
+
+
+def to_device(inp: dict, device) -> dict:
+    """Copy of a workload dict with every tensor moved to `device`."""
+    out = {}
+    for key, v in inp.items():
+        out[key] = v.to(device) if isinstance(v, torch.Tensor) else v
+    return out
