@@ -1,0 +1,515 @@
+// capi.cu -- the C ABI of include/moe.h: argument checks, workspace layout,
+// TMA descriptors, and the launch sequence of each stage.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+using namespace moe;
+
+namespace {
+
+thread_local char g_last_error[256] = "";
+
+int fail(int code, const char* fmt, const char* detail = "") {
+    snprintf(g_last_error, sizeof g_last_error, fmt, detail);
+    return code;
+}
+int fail_cuda(cudaError_t e, const char* where) {
+    snprintf(g_last_error, sizeof g_last_error, "%s: %s", where, cudaGetErrorString(e));
+    return MOE_ERR_CUDA;
+}
+
+size_t esize(const moe_cfg& c) { return c.dtype == MOE_F32 ? 4 : 2; }
+size_t align_up(size_t v) { return (v + 255) & ~(size_t)255; }
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+constexpr int kRouterTopkMaxBlocks = 1024;
+int router_blocks(int T) {
+    const int b = (T + 7) / 8;
+    return b < 1 ? 1 : (b > kRouterTopkMaxBlocks ? kRouterTopkMaxBlocks : b);
+}
+
+struct Layout {
+    size_t ctrl, tile_status, rank, prob_part, prob_mean, logits, topk_idx, topk_w, counts_pre,
+        counts_kept, offsets, perm_src, dest, drop_mask, stats, xp, h, hsh, ys, sh, total;
+};
+
+Layout layout_of(const moe_cfg& c) {
+    Layout L;
+    const size_t A = (size_t)c.T * c.k, E = c.E, T = c.T, es = esize(c);
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes); return at; };
+    L.ctrl = take(kCtrlWords * 4);
+    L.tile_status = take((size_t)dispatch_blocks((int)A) * E * 4);
+    L.rank = take(A * 4);
+    L.prob_part = take((size_t)router_blocks(c.T) * E * 4);
+    L.prob_mean = take(E * 4);
+    L.logits = take(T * E * 4);
+    L.topk_idx = take(A * 4);
+    L.topk_w = take(A * 4);
+    L.counts_pre = take(E * 4);
+    L.counts_kept = take(E * 4);
+    L.offsets = take((E + 1) * 4);
+    L.perm_src = take(A * 4);
+    L.dest = take(A * 4);
+    L.drop_mask = take(A);
+    L.stats = take(2 * 4);
+    L.xp = take(A * c.d * es);
+    L.h = take(A * c.F * es);
+    L.hsh = take(T * (size_t)c.F_shared * es);
+    L.ys = take(A * c.d * es);
+    L.sh = take(c.F_shared > 0 ? T * c.d * es : 0);
+    L.total = o;
+    return L;
+}
+
+int check_cfg(const moe_cfg* c) {
+    if (!c) return fail(MOE_ERR_INVALID_ARG, "cfg is NULL%s");
+    if (c->T < 0 || c->T > (1 << 24)) return fail(MOE_ERR_INVALID_ARG, "T out of range [0, 2^24]%s");
+    if (c->d < 8 || c->d % 8) return fail(MOE_ERR_INVALID_ARG, "d must be a positive multiple of 8%s");
+    if (c->F < 8 || c->F % 8) return fail(MOE_ERR_INVALID_ARG, "F must be a positive multiple of 8%s");
+    if (c->E < 1 || c->E > kMaxExperts) return fail(MOE_ERR_INVALID_ARG, "E must be in [1, 256]%s");
+    if (c->k < 1 || c->k > c->E || c->k > kMaxTopK)
+        return fail(MOE_ERR_INVALID_ARG, "k must be in [1, min(E, 8)]%s");
+    if ((long long)c->T * c->k > (1LL << 26)) return fail(MOE_ERR_INVALID_ARG, "T*k above 2^26%s");
+    if (c->F_shared < 0 || c->F_shared % 8)
+        return fail(MOE_ERR_INVALID_ARG, "F_shared must be 0 or a multiple of 8%s");
+    if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return fail(MOE_ERR_INVALID_ARG, "unknown dtype%s");
+    if (c->act != MOE_GELU_ERF && c->act != MOE_SWIGLU) return fail(MOE_ERR_INVALID_ARG, "unknown act%s");
+    if (c->has_bias && c->act == MOE_SWIGLU)
+        return fail(MOE_ERR_UNSUPPORTED, "SwiGLU experts take no biases%s");
+    if (c->F_shared > 0 && c->act != MOE_SWIGLU)
+        return fail(MOE_ERR_UNSUPPORTED, "the shared expert is a SwiGLU expert; needs act = SwiGLU%s");
+    if (!(c->capacity_factor == c->capacity_factor)) return fail(MOE_ERR_INVALID_ARG, "capacity_factor is NaN%s");
+    return MOE_OK;
+}
+
+int check_ws(const moe_cfg& c, const void* ws, size_t ws_bytes) {
+    if (!ws) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL%s");
+    if (!aligned16(ws)) return fail(MOE_ERR_INVALID_ARG, "workspace must be 16-byte aligned%s");
+    if (ws_bytes < layout_of(c).total) return fail(MOE_ERR_WORKSPACE, "workspace too small%s");
+    return MOE_OK;
+}
+
+// data pointer checks: non-null; bf16 row buffers 16-byte aligned (TMA and
+// 16-byte vector access); fp32 buffers too (16-byte vectors).
+int check_ptr(const void* p, const char* name) {
+    if (!p) return fail(MOE_ERR_INVALID_ARG, "%s is NULL", name);
+    if (!aligned16(p)) return fail(MOE_ERR_INVALID_ARG, "%s must be 16-byte aligned", name);
+    return MOE_OK;
+}
+int check_ptr4(const void* p, const char* name) {
+    if (!p) return fail(MOE_ERR_INVALID_ARG, "%s is NULL", name);
+    if (((uintptr_t)p & 3u) != 0) return fail(MOE_ERR_INVALID_ARG, "%s must be 4-byte aligned", name);
+    return MOE_OK;
+}
+
+#define MOE_TRY(x)                  \
+    do {                            \
+        const int _rc = (x);        \
+        if (_rc != MOE_OK) return _rc; \
+    } while (0)
+#define MOE_CUDA(x, where)                           \
+    do {                                             \
+        const cudaError_t _e = (x);                  \
+        if (_e != cudaSuccess) return fail_cuda(_e, where); \
+    } while (0)
+
+int check_weights(const moe_cfg& c, const moe_weights* w) {
+    if (!w) return fail(MOE_ERR_INVALID_ARG, "weights is NULL%s");
+    MOE_TRY(check_ptr(w->W1, "W1"));
+    MOE_TRY(check_ptr(w->W2, "W2"));
+    if (c.act == MOE_SWIGLU) MOE_TRY(check_ptr(w->W3, "W3"));
+    if (c.has_bias) {
+        MOE_TRY(check_ptr(w->b1, "b1"));
+        MOE_TRY(check_ptr(w->b2, "b2"));
+    }
+    if (c.F_shared > 0) {
+        MOE_TRY(check_ptr(w->S1, "S1"));
+        MOE_TRY(check_ptr(w->S3, "S3"));
+        MOE_TRY(check_ptr(w->S2, "S2"));
+    }
+    return MOE_OK;
+}
+
+// ---------------------------------------------------------------- devices
+struct DevInfo {
+    int num_sms = 0;
+    int cc = 0;
+};
+
+int device_info(DevInfo* out) {
+    static std::mutex mu;
+    static DevInfo cache[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(MOE_ERR_NO_DEVICE, "device ordinal out of range%s");
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev].num_sms == 0) {
+        int sms = 0, maj = 0, mnr = 0;
+        MOE_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev), "attr SMs");
+        MOE_CUDA(cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, dev), "attr cc");
+        MOE_CUDA(cudaDeviceGetAttribute(&mnr, cudaDevAttrComputeCapabilityMinor, dev), "attr cc");
+        cache[dev].num_sms = sms;
+        cache[dev].cc = maj * 10 + mnr;
+    }
+    *out = cache[dev];
+    return MOE_OK;
+}
+
+// ------------------------------------------------------------- TMA maps
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
+// bf16 row-major [rows, cols] matrix; box = 128 rows x 64 columns (128 bytes),
+// 128-byte swizzle, out-of-range elements read as zero.
+int encode_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, const char* what) {
+    auto fn = encode_fn();
+    if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled unavailable%s");
+    if (rows == 0) rows = 1;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "tensor map encode failed for %s", what);
+    return MOE_OK;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) { return reinterpret_cast<T*>(static_cast<char*>(ws) + off); }
+
+// --------------------------------------------------------------- stages
+int run_route(const moe_cfg& c, const DevInfo& di, const void* x, const void* Wr,
+              const float* bias, float* logits, int* topk_idx, float* topk_w, float* prob_mean,
+              void* ws, cudaStream_t st) {
+    const Layout L = layout_of(c);
+    MOE_CUDA(launch_router_logits_simt(c.dtype, x, Wr, bias, logits, c.T, c.d, c.E, st),
+             "router logits launch");
+    MOE_CUDA(launch_router_topk(logits, c.T, c.E, c.k, topk_idx, topk_w, at<float>(ws, L.prob_part),
+                                prob_mean, at<int>(ws, L.ctrl) + kCtrlRouterDone,
+                                router_blocks(c.T), st),
+             "router top-k launch");
+    (void)di;
+    return MOE_OK;
+}
+
+int run_dispatch(const moe_cfg& c, const DevInfo& di, const int* topk_idx, const float* prob_mean,
+                 int* counts_pre, int* counts_kept, int* offsets, int* perm_src, int* dest,
+                 unsigned char* drop_mask, float* stats, void* ws, cudaStream_t st) {
+    const Layout L = layout_of(c);
+    MOE_CUDA(launch_dispatch(topk_idx, c.T, c.k, c.E, moe_capacity(&c),
+                             at<unsigned>(ws, L.tile_status), at<int>(ws, L.ctrl),
+                             at<int>(ws, L.rank), counts_pre, counts_kept, offsets, dest, perm_src,
+                             drop_mask, prob_mean, stats, di.num_sms, st),
+             "dispatch launch");
+    return MOE_OK;
+}
+
+// ev (optional): events recorded after the gather, the up- and the
+// down-projection.
+int run_expert_ffn(const moe_cfg& c, const DevInfo& di, const void* x, const int* perm_src,
+                   const int* offsets, const float* topk_w, const moe_weights& w, void* Ys,
+                   void* Sh, void* ws, cudaStream_t st, cudaEvent_t const* ev = nullptr) {
+    const Layout L = layout_of(c);
+    int* status = at<int>(ws, L.ctrl) + kCtrlStatus;
+    const int A = c.T * c.k;
+    void* Xp = at<char>(ws, L.xp);
+    void* H = at<char>(ws, L.h);
+    void* Hsh = at<char>(ws, L.hsh);
+    const int rows_sh = c.F_shared > 0 ? c.T : 0;
+    MOE_CUDA(launch_gather(c.dtype, x, perm_src, offsets, c.E, c.k, c.T, c.d, Xp, status,
+                           di.num_sms, st),
+             "gather launch");
+    if (ev) MOE_CUDA(cudaEventRecord(ev[0], st), "event record");
+    if (c.dtype == MOE_F32) {
+        SimtFfnArgs up{};
+        up.A = (const float*)Xp; up.B = (const float*)w.W1; up.B2 = (const float*)w.W3;
+        up.bias = c.has_bias ? (const float*)w.b1 : nullptr;
+        up.offsets = offsets; up.E = c.E; up.N = c.F; up.K = c.d;
+        up.A_sh = (const float*)x; up.B_sh = (const float*)w.S1; up.B2_sh = (const float*)w.S3;
+        up.rows_sh = rows_sh; up.N_sh = c.F_shared; up.K_sh = c.d;
+        up.out = (float*)H; up.out_sh = (float*)Hsh;
+        MOE_CUDA(launch_ffn_simt(c.act == MOE_SWIGLU ? kModeSwiglu : kModeGelu, up, A, st),
+                 "fp32 up-projection launch");
+        if (ev) MOE_CUDA(cudaEventRecord(ev[1], st), "event record");
+        SimtFfnArgs dn{};
+        dn.A = (const float*)H; dn.B = (const float*)w.W2; dn.B2 = nullptr;
+        dn.bias = c.has_bias ? (const float*)w.b2 : nullptr;
+        dn.offsets = offsets; dn.E = c.E; dn.N = c.d; dn.K = c.F;
+        dn.A_sh = (const float*)Hsh; dn.B_sh = (const float*)w.S2; dn.B2_sh = nullptr;
+        dn.rows_sh = rows_sh; dn.N_sh = c.d; dn.K_sh = c.F_shared;
+        dn.out = (float*)Ys; dn.out_sh = (float*)Sh;
+        dn.perm_src = perm_src; dn.gate_w = topk_w;
+        MOE_CUDA(launch_ffn_simt(kModeDown, dn, A, st), "fp32 down-projection launch");
+        if (ev) MOE_CUDA(cudaEventRecord(ev[2], st), "event record");
+        return MOE_OK;
+    }
+    if (di.cc != 103)
+        return fail(MOE_ERR_UNSUPPORTED, "bf16 expert GEMMs need an sm_103a (B300) device%s");
+    // up-projection maps: A, B, B2, A_sh, B_sh, B2_sh
+    CUtensorMap maps[6];
+    MOE_TRY(encode_rows(&maps[0], Xp, (uint64_t)A, c.d, "gathered rows"));
+    MOE_TRY(encode_rows(&maps[1], w.W1, (uint64_t)c.E * c.F, c.d, "W1"));
+    MOE_TRY(encode_rows(&maps[2], c.act == MOE_SWIGLU ? w.W3 : w.W1, (uint64_t)c.E * c.F, c.d, "W3"));
+    if (rows_sh) {
+        MOE_TRY(encode_rows(&maps[3], x, (uint64_t)c.T, c.d, "x"));
+        MOE_TRY(encode_rows(&maps[4], w.S1, (uint64_t)c.F_shared, c.d, "S1"));
+        MOE_TRY(encode_rows(&maps[5], w.S3, (uint64_t)c.F_shared, c.d, "S3"));
+    } else {
+        maps[3] = maps[0]; maps[4] = maps[1]; maps[5] = maps[2];
+    }
+    TcFfnArgs up{};
+    up.offsets = offsets; up.E = c.E; up.rows_sh = rows_sh;
+    up.N = c.F; up.K = c.d; up.N_sh = c.F_shared; up.K_sh = c.d;
+    up.out = H; up.out_sh = Hsh;
+    up.bias = c.has_bias ? (const __nv_bfloat16*)w.b1 : nullptr;
+    up.status = status;
+    MOE_CUDA(launch_ffn_tc(c.act == MOE_SWIGLU ? kModeSwiglu : kModeGelu, maps, up, di.num_sms, st),
+             "up-projection launch");
+    if (ev) MOE_CUDA(cudaEventRecord(ev[1], st), "event record");
+    // down-projection maps
+    MOE_TRY(encode_rows(&maps[0], H, (uint64_t)A, c.F, "hidden rows"));
+    MOE_TRY(encode_rows(&maps[1], w.W2, (uint64_t)c.E * c.d, c.F, "W2"));
+    maps[2] = maps[1];
+    if (rows_sh) {
+        MOE_TRY(encode_rows(&maps[3], Hsh, (uint64_t)c.T, c.F_shared, "shared hidden rows"));
+        MOE_TRY(encode_rows(&maps[4], w.S2, (uint64_t)c.d, c.F_shared, "S2"));
+        maps[5] = maps[4];
+    } else {
+        maps[3] = maps[0]; maps[4] = maps[1]; maps[5] = maps[2];
+    }
+    TcFfnArgs dn{};
+    dn.offsets = offsets; dn.E = c.E; dn.rows_sh = rows_sh;
+    dn.N = c.d; dn.K = c.F; dn.N_sh = c.d; dn.K_sh = c.F_shared;
+    dn.out = Ys; dn.out_sh = Sh;
+    dn.bias = c.has_bias ? (const __nv_bfloat16*)w.b2 : nullptr;
+    dn.perm_src = perm_src; dn.gate_w = topk_w;
+    dn.status = status;
+    MOE_CUDA(launch_ffn_tc(kModeDown, maps, dn, di.num_sms, st), "down-projection launch");
+    if (ev) MOE_CUDA(cudaEventRecord(ev[2], st), "event record");
+    return MOE_OK;
+}
+
+}  // namespace
+
+// ====================================================================== ABI
+extern "C" {
+
+const char* moe_status_string(int status) {
+    switch (status) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+        case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+        case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+        case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT";
+        case MOE_ERR_DEVICE_BOUNDS: return "MOE_ERR_DEVICE_BOUNDS";
+        case MOE_ERR_NO_DEVICE: return "MOE_ERR_NO_DEVICE";
+        default: return "MOE_ERR_UNKNOWN";
+    }
+}
+
+const char* moe_last_error(void) { return g_last_error; }
+
+long long moe_capacity(const moe_cfg* cfg) {
+    if (!cfg || cfg->E < 1) return -1;
+    if (!(cfg->capacity_factor > 0.f)) return -1;
+    const double ideal = (double)cfg->T * (double)cfg->k / (double)cfg->E;
+    const long long cap = (long long)floor(ideal * (double)cfg->capacity_factor);
+    return cap < 1 ? 1 : cap;
+}
+
+int moe_workspace_size(const moe_cfg* cfg, size_t* bytes) {
+    MOE_TRY(check_cfg(cfg));
+    if (!bytes) return fail(MOE_ERR_INVALID_ARG, "bytes is NULL%s");
+    *bytes = layout_of(*cfg).total;
+    return MOE_OK;
+}
+
+int moe_workspace_init(const moe_cfg* cfg, void* ws, size_t ws_bytes, void* stream) {
+    MOE_TRY(check_cfg(cfg));
+    MOE_TRY(check_ws(*cfg, ws, ws_bytes));
+    const Layout L = layout_of(*cfg);
+    MOE_CUDA(cudaMemsetAsync(ws, 0, L.rank, (cudaStream_t)stream), "workspace init");
+    return MOE_OK;
+}
+
+int moe_route(const moe_cfg* cfg, const void* x, const void* Wr, const float* logit_bias,
+              float* logits, int* topk_idx, float* topk_w, float* prob_mean, void* ws,
+              size_t ws_bytes, void* stream) {
+    MOE_TRY(check_cfg(cfg));
+    MOE_TRY(check_ws(*cfg, ws, ws_bytes));
+    if (cfg->T == 0) return MOE_OK;
+    MOE_TRY(check_ptr(x, "x"));
+    MOE_TRY(check_ptr(Wr, "Wr"));
+    if (logit_bias) MOE_TRY(check_ptr4(logit_bias, "logit_bias"));
+    MOE_TRY(check_ptr4(logits, "logits"));
+    MOE_TRY(check_ptr4(topk_idx, "topk_idx"));
+    MOE_TRY(check_ptr4(topk_w, "topk_w"));
+    if (prob_mean) MOE_TRY(check_ptr4(prob_mean, "prob_mean"));
+    DevInfo di;
+    MOE_TRY(device_info(&di));
+    return run_route(*cfg, di, x, Wr, logit_bias, logits, topk_idx, topk_w, prob_mean, ws,
+                     (cudaStream_t)stream);
+}
+
+int moe_dispatch(const moe_cfg* cfg, const int* topk_idx, const float* prob_mean, int* counts_pre,
+                 int* counts_kept, int* offsets, int* perm_src, int* dest,
+                 unsigned char* drop_mask, float* stats, void* ws, size_t ws_bytes, void* stream) {
+    MOE_TRY(check_cfg(cfg));
+    MOE_TRY(check_ws(*cfg, ws, ws_bytes));
+    MOE_TRY(check_ptr4(counts_pre, "counts_pre"));
+    MOE_TRY(check_ptr4(counts_kept, "counts_kept"));
+    MOE_TRY(check_ptr4(offsets, "offsets"));
+    if (cfg->T == 0) return MOE_OK;
+    MOE_TRY(check_ptr4(topk_idx, "topk_idx"));
+    MOE_TRY(check_ptr4(perm_src, "perm_src"));
+    MOE_TRY(check_ptr4(dest, "dest"));
+    if (!drop_mask) return fail(MOE_ERR_INVALID_ARG, "drop_mask is NULL%s");
+    if (stats) MOE_TRY(check_ptr4(stats, "stats"));
+    DevInfo di;
+    MOE_TRY(device_info(&di));
+    return run_dispatch(*cfg, di, topk_idx, prob_mean, counts_pre, counts_kept, offsets, perm_src,
+                        dest, drop_mask, stats, ws, (cudaStream_t)stream);
+}
+
+int moe_expert_ffn(const moe_cfg* cfg, const void* x, const int* perm_src, const int* offsets,
+                   const float* topk_w, const moe_weights* w, void* Ys, void* shared_out, void* ws,
+                   size_t ws_bytes, void* stream) {
+    MOE_TRY(check_cfg(cfg));
+    MOE_TRY(check_ws(*cfg, ws, ws_bytes));
+    if (cfg->T == 0) return MOE_OK;
+    MOE_TRY(check_ptr(x, "x"));
+    MOE_TRY(check_ptr4(perm_src, "perm_src"));
+    MOE_TRY(check_ptr4(offsets, "offsets"));
+    MOE_TRY(check_ptr4(topk_w, "topk_w"));
+    MOE_TRY(check_weights(*cfg, w));
+    MOE_TRY(check_ptr(Ys, "Ys"));
+    if (cfg->F_shared > 0) MOE_TRY(check_ptr(shared_out, "shared_out"));
+    DevInfo di;
+    MOE_TRY(device_info(&di));
+    return run_expert_ffn(*cfg, di, x, perm_src, offsets, topk_w, *w, Ys,
+                          cfg->F_shared > 0 ? shared_out : nullptr, ws, (cudaStream_t)stream);
+}
+
+int moe_combine(const moe_cfg* cfg, const void* x, const void* Ys, const unsigned char* drop_mask,
+                const void* shared_out, void* y, void* stream) {
+    MOE_TRY(check_cfg(cfg));
+    if (cfg->T == 0) return MOE_OK;
+    MOE_TRY(check_ptr(x, "x"));
+    MOE_TRY(check_ptr(Ys, "Ys"));
+    MOE_TRY(check_ptr(y, "y"));
+    if (!drop_mask) return fail(MOE_ERR_INVALID_ARG, "drop_mask is NULL%s");
+    if (shared_out) MOE_TRY(check_ptr(shared_out, "shared_out"));
+    DevInfo di;
+    MOE_TRY(device_info(&di));
+    MOE_CUDA(launch_combine(cfg->dtype, x, Ys, drop_mask, shared_out, y, cfg->T, cfg->d, cfg->k,
+                            di.num_sms, (cudaStream_t)stream),
+             "combine launch");
+    return MOE_OK;
+}
+
+static int layer_forward_impl(const moe_cfg* cfg, const void* x, const void* Wr,
+                              const float* logit_bias, const moe_weights* w,
+                              const moe_layer_out* out, void* ws, size_t ws_bytes, void* stream,
+                              void* const* events) {
+    MOE_TRY(check_cfg(cfg));
+    MOE_TRY(check_ws(*cfg, ws, ws_bytes));
+    if (!out) return fail(MOE_ERR_INVALID_ARG, "out is NULL%s");
+    if (cfg->T == 0) return MOE_OK;
+    const moe_cfg& c = *cfg;
+    MOE_TRY(check_ptr(x, "x"));
+    MOE_TRY(check_ptr(Wr, "Wr"));
+    if (logit_bias) MOE_TRY(check_ptr4(logit_bias, "logit_bias"));
+    MOE_TRY(check_weights(c, w));
+    MOE_TRY(check_ptr(out->y, "y"));
+    if (out->logits) MOE_TRY(check_ptr4(out->logits, "logits"));
+    if (out->topk_idx) MOE_TRY(check_ptr4(out->topk_idx, "topk_idx"));
+    if (out->topk_w) MOE_TRY(check_ptr4(out->topk_w, "topk_w"));
+    if (out->counts_pre) MOE_TRY(check_ptr4(out->counts_pre, "counts_pre"));
+    if (out->counts_kept) MOE_TRY(check_ptr4(out->counts_kept, "counts_kept"));
+    if (out->stats) MOE_TRY(check_ptr4(out->stats, "stats"));
+    DevInfo di;
+    MOE_TRY(device_info(&di));
+    const Layout L = layout_of(c);
+    cudaStream_t st = (cudaStream_t)stream;
+    float* logits = out->logits ? out->logits : at<float>(ws, L.logits);
+    int* topk_idx = out->topk_idx ? out->topk_idx : at<int>(ws, L.topk_idx);
+    float* topk_w = out->topk_w ? out->topk_w : at<float>(ws, L.topk_w);
+    int* counts_pre = out->counts_pre ? out->counts_pre : at<int>(ws, L.counts_pre);
+    int* counts_kept = out->counts_kept ? out->counts_kept : at<int>(ws, L.counts_kept);
+    unsigned char* drop = out->drop_mask ? out->drop_mask : at<unsigned char>(ws, L.drop_mask);
+    float* stats = out->stats ? out->stats : at<float>(ws, L.stats);
+    float* prob_mean = at<float>(ws, L.prob_mean);
+    int* offsets = at<int>(ws, L.offsets);
+    int* perm_src = at<int>(ws, L.perm_src);
+    int* dest = at<int>(ws, L.dest);
+    void* Ys = at<char>(ws, L.ys);
+    void* Sh = c.F_shared > 0 ? at<char>(ws, L.sh) : nullptr;
+    cudaEvent_t const* ev = reinterpret_cast<cudaEvent_t const*>(events);
+    if (ev) MOE_CUDA(cudaEventRecord(ev[0], st), "event record");
+    MOE_TRY(run_route(c, di, x, Wr, logit_bias, logits, topk_idx, topk_w, prob_mean, ws, st));
+    if (ev) MOE_CUDA(cudaEventRecord(ev[1], st), "event record");
+    MOE_TRY(run_dispatch(c, di, topk_idx, prob_mean, counts_pre, counts_kept, offsets, perm_src,
+                         dest, drop, stats, ws, st));
+    if (ev) MOE_CUDA(cudaEventRecord(ev[2], st), "event record");
+    MOE_TRY(run_expert_ffn(c, di, x, perm_src, offsets, topk_w, *w, Ys, Sh, ws, st,
+                           ev ? ev + 3 : nullptr));
+    MOE_CUDA(launch_combine(c.dtype, x, Ys, drop, Sh, out->y, c.T, c.d, c.k, di.num_sms, st),
+             "combine launch");
+    if (ev) MOE_CUDA(cudaEventRecord(ev[6], st), "event record");
+    return MOE_OK;
+}
+
+int moe_layer_forward(const moe_cfg* cfg, const void* x, const void* Wr, const float* logit_bias,
+                      const moe_weights* w, const moe_layer_out* out, void* ws, size_t ws_bytes,
+                      void* stream) {
+    return layer_forward_impl(cfg, x, Wr, logit_bias, w, out, ws, ws_bytes, stream, nullptr);
+}
+
+int moe_layer_forward_profiled(const moe_cfg* cfg, const void* x, const void* Wr,
+                               const float* logit_bias, const moe_weights* w,
+                               const moe_layer_out* out, void* ws, size_t ws_bytes, void* stream,
+                               void* const* events) {
+    if (!events) return fail(MOE_ERR_INVALID_ARG, "events is NULL%s");
+    for (int i = 0; i < 7; ++i)
+        if (!events[i]) return fail(MOE_ERR_INVALID_ARG, "events[i] is NULL%s");
+    return layer_forward_impl(cfg, x, Wr, logit_bias, w, out, ws, ws_bytes, stream, events);
+}
+
+int moe_get_device_status(void* ws, size_t ws_bytes, void* stream, int* status) {
+    if (!ws || !status) return fail(MOE_ERR_INVALID_ARG, "ws/status is NULL%s");
+    if (ws_bytes < kCtrlWords * 4) return fail(MOE_ERR_WORKSPACE, "workspace too small%s");
+    int v = 0;
+    MOE_CUDA(cudaMemcpyAsync(&v, at<int>(ws, 0) + kCtrlStatus, sizeof v, cudaMemcpyDeviceToHost,
+                             (cudaStream_t)stream),
+             "status read");
+    MOE_CUDA(cudaStreamSynchronize((cudaStream_t)stream), "status sync");
+    *status = v;
+    return MOE_OK;
+}
+
+}  // extern "C"

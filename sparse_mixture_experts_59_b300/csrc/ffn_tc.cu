@@ -1,0 +1,365 @@
+// ffn_tc.cu -- bf16 grouped expert GEMMs on the 5th-generation tensor cores.
+//
+// "How Mixture of Experts Works": production layers run every expert's rows
+// as grouped GEMMs instead of a per-expert loop (remark after the MoELayer
+// listing); "Mixture of Experts (MoE)", "Implementing a complete MoE layer":
+// SwiGLU experts w_down(silu(w_gate x) * w_up x); "Mixture-of-Experts
+// Routing", "How a sparse MoE layer works": GELU MLP experts with biases.
+//
+// One persistent kernel per projection.  Its tiles cover every (group,
+// row-tile, column-tile) of the ragged expert segments -- read on the device
+// from `offsets`, so no host sync -- plus, when present, the shared expert as
+// one more group whose rows are the T tokens.  Per CTA (one per SM):
+//   warp 0      TMA producer: A tile 128x64 and B tile 256x64 (bf16, 128B
+//               swizzle) per stage into a 4-deep shared-memory ring;
+//   warp 1      allocates 512 TMEM columns and issues tcgen05.mma
+//               (M=128, N=256, K=16) from one thread into one of two
+//               accumulators (2 x 256 fp32 columns);
+//   warps 2-5   epilogue: tcgen05.ld the accumulator (warp w reads TMEM lanes
+//               32*(w%4)..+31, i.e. tile rows), apply the fused epilogue and
+//               store bf16 rows; the second accumulator lets the next tile's
+//               MMAs run meanwhile.
+// Epilogues:
+//   kModeSwiglu  B = 128 gate rows then 128 up rows of the same hidden units,
+//                so one MMA gives [g | u];  H = silu(g) * u        (128 cols/tile)
+//   kModeGelu    H = gelu_erf(acc + b1)                             (256 cols/tile)
+//   kModeDown    Ys[perm_src[r]] = topk_w[perm_src[r]] * (acc + b2), i.e. the
+//                gate scale and the scatter back to the assignment slot;
+//                shared group: Sh[t] = acc                          (256 cols/tile)
+// Rows past a segment's end and columns past N are computed on whatever the
+// tile reads (the next segment, or TMA's zero fill) and never stored.
+#include "common.cuh"
+#include "kernels.cuh"
+#include "tc_ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int BM = 128;        // tile rows = MMA M
+constexpr int BK = 64;         // bf16 elements per 128-byte swizzled row
+constexpr int MMA_N = 256;     // B rows per stage
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;        // 16 KB
+constexpr int B_BYTES = MMA_N * BK * 2;     // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int TMEM_COLS = 512;              // two 256-column accumulators
+constexpr int NUM_THREADS = 192;
+constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, MMA_N);
+
+// shared-memory carve-up (offsets from the 1024-aligned base)
+constexpr int OFF_A = 0;
+constexpr int OFF_B = STAGES * A_BYTES;
+constexpr int OFF_BAR = OFF_B + STAGES * B_BYTES;
+constexpr int NUM_BARS = 2 * STAGES + 2 + 2 + 1;
+constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;          // tmem base, abort flag
+constexpr int OFF_START = OFF_MISC + 16;                  // group tile starts
+constexpr int OFF_OFFS = OFF_START + (kMaxExperts + 2) * 4;  // cached offsets
+constexpr int SMEM_USED = OFF_OFFS + (kMaxExperts + 2) * 4;
+constexpr int SMEM_BYTES = SMEM_USED + 1024;              // alignment slack
+
+template <int MODE> struct ModeTraits;
+template <> struct ModeTraits<kModeSwiglu> { static constexpr int BN_OUT = 128; };
+template <> struct ModeTraits<kModeGelu> { static constexpr int BN_OUT = 256; };
+template <> struct ModeTraits<kModeDown> { static constexpr int BN_OUT = 256; };
+
+struct Tile {
+    int g;          // group (E = shared expert)
+    bool sh;
+    int arow;       // first A row of the tile in its tensor map
+    int row_end;    // one past the segment's last A row
+    int n0;         // first output column
+    int wrow0, wrow1;  // weight rows of the two 128-row B boxes
+    int N, nk;
+};
+
+template <int MODE>
+__device__ __forceinline__ Tile decode_tile(const TcFfnArgs& p, const int* s_start,
+                                            const int* s_off, int G, int tile) {
+    constexpr int BN_OUT = ModeTraits<MODE>::BN_OUT;
+    Tile t;
+    t.g = find_group(s_start, G, tile);
+    t.sh = (t.g == p.E);
+    const int seg0 = t.sh ? 0 : s_off[t.g];
+    const int rows = t.sh ? p.rows_sh : s_off[t.g + 1] - seg0;
+    const int mt = (rows + BM - 1) / BM;
+    const int local = tile - s_start[t.g];
+    const int n = local / mt, m = local - (local / mt) * mt;
+    t.arow = seg0 + m * BM;
+    t.row_end = seg0 + rows;
+    t.N = t.sh ? p.N_sh : p.N;
+    const int K = t.sh ? p.K_sh : p.K;
+    t.nk = (K + BK - 1) / BK;
+    t.n0 = n * BN_OUT;
+    const int wbase = t.sh ? 0 : t.g * p.N;
+    if (MODE == kModeSwiglu) {
+        t.wrow0 = wbase + t.n0;      // gate rows (map B)
+        t.wrow1 = wbase + t.n0;      // up rows   (map B2)
+    } else {
+        t.wrow0 = wbase + t.n0;
+        t.wrow1 = wbase + t.n0 + 128;
+    }
+    return t;
+}
+
+__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const float (&v)[32], int ncols) {
+    // ncols = number of valid columns in this 32-wide chunk (multiple of 8)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        if (q * 8 < ncols) {
+            uint4 pk = make_uint4(pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]),
+                                  pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]),
+                                  pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]),
+                                  pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]));
+            reinterpret_cast<uint4*>(dst)[q] = pk;
+        }
+    }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+              const __grid_constant__ CUtensorMap mapB2, const __grid_constant__ CUtensorMap mapA_sh,
+              const __grid_constant__ CUtensorMap mapB_sh,
+              const __grid_constant__ CUtensorMap mapB2_sh, const TcFfnArgs p) {
+    constexpr int BN_OUT = ModeTraits<MODE>::BN_OUT;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* sA = smem + OFF_A;
+    uint8_t* sB = smem + OFF_B;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + STAGES;
+    uint64_t* tfull = bars + 2 * STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+    int* s_start = reinterpret_cast<int*>(smem + OFF_START);
+    int* s_off = reinterpret_cast<int*>(smem + OFF_OFFS);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(&full[s], 1);
+            ptx::mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            ptx::mbar_init(&tfull[a], 1);
+            ptx::mbar_init(&tempty[a], 128);
+        }
+        ptx::mbar_init(drain, 1);
+        *s_abort = 0;
+        ptx::fence_mbarrier_init();
+        ptx::prefetch_tensormap(&mapA);
+        ptx::prefetch_tensormap(&mapB);
+        ptx::prefetch_tensormap(&mapB2);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(s_tmem, TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    for (int i = threadIdx.x; i <= p.E; i += NUM_THREADS) s_off[i] = p.offsets[i];
+    const int nt_r = (p.N + BN_OUT - 1) / BN_OUT;
+    const int nt_s = p.rows_sh > 0 ? (p.N_sh + BN_OUT - 1) / BN_OUT : 0;
+    group_tile_prefix(p.offsets, p.E, p.rows_sh, BM, nt_r, nt_s, s_start);
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *s_tmem;
+    const int G = p.E + (p.rows_sh > 0 ? 1 : 0);
+    const int total = s_start[G];
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+                const Tile t = decode_tile<MODE>(p, s_start, s_off, G, tile);
+                const CUtensorMap* mA = t.sh ? &mapA_sh : &mapA;
+                const CUtensorMap* mB0 = t.sh ? &mapB_sh : &mapB;
+                const CUtensorMap* mB1 = (MODE == kModeSwiglu) ? (t.sh ? &mapB2_sh : &mapB2) : mB0;
+                for (int kb = 0; kb < t.nk; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+                    if (!ptx::mbar_wait(&empty[s], ph ^ 1u, s_abort)) { ok = false; break; }
+                    ptx::mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
+                    ptx::tma_load_2d(sA + s * A_BYTES, mA, &full[s], kb * BK, t.arow);
+                    ptx::tma_load_2d(sB + s * B_BYTES, mB0, &full[s], kb * BK, t.wrow0);
+                    ptx::tma_load_2d(sB + s * B_BYTES + B_BYTES / 2, mB1, &full[s], kb * BK, t.wrow1);
+                }
+            }
+            if (!ok) {
+                *s_abort = 1;
+                raise_error(p.status, MOE_ERR_DEVICE_TIMEOUT);
+            }
+            // let this thread's copies land before the CTA can exit
+            for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
+                ptx::mbar_wait(&full[j % STAGES], (uint32_t)(j / STAGES) & 1u, nullptr);
+        }
+    } else if (warp == 1) {
+        // -------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            int it = 0, tc = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++tc) {
+                const Tile t = decode_tile<MODE>(p, s_start, s_off, G, tile);
+                const int acc = tc & 1;
+                const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
+                if (!ptx::mbar_wait(&tempty[acc], aph ^ 1u, s_abort)) { ok = false; break; }
+                ptx::tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * MMA_N);
+                for (int kb = 0; kb < t.nk; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+                    if (!ptx::mbar_wait(&full[s], ph, s_abort)) { ok = false; break; }
+                    ptx::tc_fence_after();
+                    const uint64_t ad = ptx::sw128_desc(ptx::smem_u32(sA + s * A_BYTES));
+                    const uint64_t bd = ptx::sw128_desc(ptx::smem_u32(sB + s * B_BYTES));
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)   // +32 bytes along K per step
+                        ptx::mma_bf16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2),
+                                      IDESC, (kb | kk) != 0 ? 1u : 0u);
+                    ptx::mma_commit(&empty[s]);
+                }
+                if (!ok) break;
+                ptx::mma_commit(&tfull[acc]);
+            }
+            if (!ok) {
+                *s_abort = 1;
+                raise_error(p.status, MOE_ERR_DEVICE_TIMEOUT);
+            }
+            // every MMA issued by this thread completes before TMEM is freed
+            ptx::mma_commit(drain);
+            ptx::mbar_wait(drain, 0, nullptr);
+        }
+    } else {
+        // ---------------------------------------------------------- epilogue
+        const int q = warp & 3;                 // TMEM lane quadrant of this warp
+        const int row_in_tile = q * 32 + lane;
+        int tc = 0;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++tc) {
+            const Tile t = decode_tile<MODE>(p, s_start, s_off, G, tile);
+            const int acc = tc & 1;
+            const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
+            int ok = 1;
+            if (lane == 0) ok = ptx::mbar_wait(&tfull[acc], aph, s_abort) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) {
+                    *s_abort = 1;
+                    raise_error(p.status, MOE_ERR_DEVICE_TIMEOUT);
+                }
+                break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t taddr = tmem_base + (uint32_t)(acc * MMA_N) + ((uint32_t)(q * 32) << 16);
+            const int r = t.arow + row_in_tile;
+            const bool row_ok = r < t.row_end;
+
+            if (MODE == kModeSwiglu) {
+                __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(t.sh ? p.out_sh : p.out) +
+                                     (size_t)r * t.N + t.n0;
+#pragma unroll 1
+                for (int c = 0; c < BN_OUT; c += 32) {
+                    __syncwarp();
+                    float g[32], u[32];
+                    ptx::tmem_ld32(taddr + c, g);
+                    ptx::tmem_ld32(taddr + 128 + c, u);
+                    const int ncols = t.N - (t.n0 + c);
+                    if (row_ok && ncols > 0) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) g[j] = silu(g[j]) * u[j];
+                        store_row32(dst + c, g, ncols);
+                    }
+                }
+            } else if (MODE == kModeGelu) {
+                __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(t.sh ? p.out_sh : p.out) +
+                                     (size_t)r * t.N + t.n0;
+                const __nv_bfloat16* bias = (p.bias && !t.sh) ? p.bias + (size_t)t.g * t.N : nullptr;
+#pragma unroll 1
+                for (int c = 0; c < BN_OUT; c += 32) {
+                    __syncwarp();
+                    float v[32];
+                    ptx::tmem_ld32(taddr + c, v);
+                    const int ncols = t.N - (t.n0 + c);
+                    if (row_ok && ncols > 0) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int n = t.n0 + c + j;
+                            const float b = (bias && n < t.N) ? __bfloat162float(bias[n]) : 0.f;
+                            v[j] = gelu_erf(v[j] + b);
+                        }
+                        store_row32(dst + c, v, ncols);
+                    }
+                }
+            } else {   // kModeDown
+                __nv_bfloat16* dst = nullptr;
+                float scale = 1.f;
+                if (row_ok) {
+                    if (t.sh) {
+                        dst = reinterpret_cast<__nv_bfloat16*>(p.out_sh) + (size_t)r * t.N + t.n0;
+                    } else {
+                        const int a = p.perm_src[r];
+                        scale = p.gate_w[a];
+                        dst = reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t)a * t.N + t.n0;
+                    }
+                }
+                const __nv_bfloat16* bias = (p.bias && !t.sh) ? p.bias + (size_t)t.g * t.N : nullptr;
+#pragma unroll 1
+                for (int c = 0; c < BN_OUT; c += 32) {
+                    __syncwarp();
+                    float v[32];
+                    ptx::tmem_ld32(taddr + c, v);
+                    const int ncols = t.N - (t.n0 + c);
+                    if (row_ok && ncols > 0) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int n = t.n0 + c + j;
+                            const float b = (bias && n < t.N) ? __bfloat162float(bias[n]) : 0.f;
+                            v[j] = scale * (v[j] + b);
+                        }
+                        store_row32(dst + c, v, ncols);
+                    }
+                }
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&tempty[acc]);
+        }
+    }
+
+    // teardown: all roles done (or aborted); free TMEM
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+}  // namespace
+
+int ffn_tc_smem_bytes() { return SMEM_BYTES; }
+
+cudaError_t launch_ffn_tc(int mode, const CUtensorMap* maps, const TcFfnArgs& p, int num_sms,
+                          cudaStream_t st) {
+    cudaError_t err;
+    const dim3 grid(num_sms), block(NUM_THREADS);
+#define MOE_TC_LAUNCH(M)                                                                        \
+    err = cudaFuncSetAttribute(ffn_tc_kernel<M>, cudaFuncAttributeMaxDynamicSharedMemorySize,   \
+                               SMEM_BYTES);                                                     \
+    if (err != cudaSuccess) return err;                                                         \
+    ffn_tc_kernel<M><<<grid, block, SMEM_BYTES, st>>>(maps[0], maps[1], maps[2], maps[3],       \
+                                                      maps[4], maps[5], p);
+    if (mode == kModeSwiglu) { MOE_TC_LAUNCH(kModeSwiglu) }
+    else if (mode == kModeGelu) { MOE_TC_LAUNCH(kModeGelu) }
+    else { MOE_TC_LAUNCH(kModeDown) }
+#undef MOE_TC_LAUNCH
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,80 @@
+// kernels.cuh -- launchers of the MoE kernels, called by the C ABI in capi.cu.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+// epilogue / activation modes of the grouped FFN kernels
+enum FfnMode { kModeSwiglu = 0, kModeGelu = 1, kModeDown = 2 };
+
+// dispatch geometry: assignments per block
+constexpr int kDspItems = 8;
+constexpr int kDspChunk = 256 * kDspItems;
+inline int dispatch_blocks(int A) { return A > 0 ? (A + kDspChunk - 1) / kDspChunk : 1; }
+
+// route.cu
+cudaError_t launch_router_logits_simt(int dtype, const void* x, const void* Wr, const float* bias,
+                                      float* logits, int T, int d, int E, cudaStream_t st);
+int router_topk_blocks(int T, int num_sms);
+cudaError_t launch_router_topk(const float* logits, int T, int E, int k, int* topk_idx,
+                               float* topk_w, float* prob_part, float* prob_mean, int* done,
+                               int nblocks, cudaStream_t st);
+
+// dispatch.cu
+cudaError_t launch_dispatch(const int* topk_idx, int T, int k, int E, long long cap,
+                            unsigned* tile_status, int* ctrl, int* rank, int* counts_pre,
+                            int* counts_kept, int* offsets, int* dest, int* perm_src,
+                            unsigned char* drop_mask, const float* prob_mean, float* stats,
+                            int num_sms, cudaStream_t st);
+
+// permute.cu
+cudaError_t launch_gather(int dtype, const void* x, const int* perm_src, const int* offsets, int E,
+                          int k, int T, int d, void* Xp, int* status, int num_sms,
+                          cudaStream_t st);
+cudaError_t launch_combine(int dtype, const void* x, const void* Ys, const unsigned char* drop_mask,
+                           const void* Sh, void* y, int T, int d, int k, int num_sms,
+                           cudaStream_t st);
+
+// ffn_simt.cu (fp32)
+struct SimtFfnArgs {
+    const float* A;           // routed rows [*, K]
+    const float* B;           // [E, N, K]
+    const float* B2;          // [E, N, K] (SwiGLU up) or null
+    const float* bias;        // [E, N] or null
+    const int* offsets;       // [E+1]
+    int E, N, K;
+    const float* A_sh;        // shared-expert rows [rows_sh, K_sh]
+    const float* B_sh;
+    const float* B2_sh;
+    int rows_sh, N_sh, K_sh;
+    float* out;               // up: H [*, N]; down: Ys [T*k, N]
+    float* out_sh;            // up: H_sh; down: Sh
+    const int* perm_src;      // down
+    const float* gate_w;      // down
+};
+cudaError_t launch_ffn_simt(int mode, const SimtFfnArgs& p, int A_rows, cudaStream_t st);
+
+// ffn_tc.cu (bf16, tcgen05)
+struct TcFfnArgs {
+    const int* offsets;       // [E+1] segment starts (routed groups)
+    int E;
+    int rows_sh;              // shared-expert rows (0 = no shared group)
+    int N, K;                 // routed output columns / reduction length
+    int N_sh, K_sh;           // shared group
+    void* out;                // bf16: up H [*, N]; down Ys [T*k, N]
+    void* out_sh;             // bf16: up H_sh [T, N_sh]; down Sh [T, N_sh]
+    const __nv_bfloat16* bias;  // [E, N] (GELU b1 / down b2) or null
+    const int* perm_src;      // down
+    const float* gate_w;      // down
+    int* status;
+};
+int ffn_tc_smem_bytes();
+// maps: A, B, B2, A_sh, B_sh, B2_sh (see ffn_tc.cu)
+cudaError_t launch_ffn_tc(int mode, const CUtensorMap* maps, const TcFfnArgs& p, int num_sms,
+                          cudaStream_t st);
+
+}  // namespace moe

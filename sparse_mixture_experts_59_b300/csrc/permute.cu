@@ -1,0 +1,109 @@
+// permute.cu -- gather of token rows into expert-grouped order, and the
+// gate-weighted combine back into token order with the residual.
+//
+// "How Mixture of Experts Works", MoELayer listing: expert_input =
+// hidden_states[token_indices] (the gather) and output.index_add_ of the
+// weight-scaled expert outputs (the combine); "Mixture-of-Experts Routing",
+// "How a sparse MoE layer works": the weighted sum is added through the
+// residual.  Both kernels move whole rows with 16-byte vectors; they are
+// bandwidth-bound and carry no arithmetic beyond the fp32 sum of the combine.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace moe {
+
+// Xp[r] = x[perm_src[r] / k] for r < R = offsets[E] (read on the device).
+// One warp per row, 16-byte vectors.
+__global__ void __launch_bounds__(256)
+gather_rows_kernel(const uint4* __restrict__ x, const int* __restrict__ perm_src,
+                   const int* __restrict__ offsets, int E, int k, int Ttok, int vec_per_row,
+                   uint4* __restrict__ Xp, int* __restrict__ status) {
+    const int R = offsets[E];
+    const int warps = (gridDim.x * blockDim.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < R; r += warps) {
+        const int a = perm_src[r];
+        const int t = a / k;
+        if (a < 0 || t >= Ttok) {
+            if (lane == 0) raise_error(status, MOE_ERR_DEVICE_BOUNDS);
+            continue;
+        }
+        const uint4* src = x + (size_t)t * vec_per_row;
+        uint4* dst = Xp + (size_t)r * vec_per_row;
+        for (int v = lane; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+    }
+}
+
+// y[t] = x[t] + sum_{s kept} Ys[t*k+s] (+ Sh[t]); fp32 sum in slot order, then
+// the shared expert, then the residual, rounded once.
+template <typename T>
+__global__ void __launch_bounds__(256)
+combine_kernel(const T* __restrict__ x, const T* __restrict__ Ys,
+               const unsigned char* __restrict__ drop_mask, const T* __restrict__ Sh,
+               T* __restrict__ y, int Ttok, int d, int k) {
+    constexpr int NV = Vec16<T>::N;
+    const int vec_per_row = d / NV;
+    const long long total = (long long)Ttok * vec_per_row;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int t = (int)(i / vec_per_row);
+        const int v = (int)(i - (long long)t * vec_per_row);
+        float acc[NV];
+#pragma unroll
+        for (int j = 0; j < NV; ++j) acc[j] = 0.f;
+        for (int s = 0; s < k; ++s) {
+            const long long a = (long long)t * k + s;
+            if (drop_mask[a]) continue;
+            float f[NV];
+            unpack16(__ldg(reinterpret_cast<const uint4*>(Ys + a * d) + v), f);
+#pragma unroll
+            for (int j = 0; j < NV; ++j) acc[j] += f[j];
+        }
+        if (Sh) {
+            float f[NV];
+            unpack16(__ldg(reinterpret_cast<const uint4*>(Sh + (size_t)t * d) + v), f);
+#pragma unroll
+            for (int j = 0; j < NV; ++j) acc[j] += f[j];
+        }
+        float xf[NV];
+        unpack16(__ldg(reinterpret_cast<const uint4*>(x + (size_t)t * d) + v), xf);
+#pragma unroll
+        for (int j = 0; j < NV; ++j) acc[j] += xf[j];
+        reinterpret_cast<uint4*>(y + (size_t)t * d)[v] = pack16(acc);
+    }
+}
+
+cudaError_t launch_gather(int dtype, const void* x, const int* perm_src, const int* offsets, int E,
+                          int k, int T, int d, void* Xp, int* status, int num_sms,
+                          cudaStream_t st) {
+    const int esize = dtype == MOE_F32 ? 4 : 2;
+    const int vpr = d * esize / 16;
+    const int A = T * k;
+    long long blocks = ((long long)A * 32 + 255) / 256;
+    if (blocks > num_sms * 16) blocks = num_sms * 16;
+    if (blocks < 1) blocks = 1;
+    gather_rows_kernel<<<(int)blocks, 256, 0, st>>>((const uint4*)x, perm_src, offsets, E, k, T, vpr,
+                                                    (uint4*)Xp, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(int dtype, const void* x, const void* Ys, const unsigned char* drop_mask,
+                           const void* Sh, void* y, int T, int d, int k, int num_sms,
+                           cudaStream_t st) {
+    const int esize = dtype == MOE_F32 ? 4 : 2;
+    const long long total = (long long)T * (d * esize / 16);
+    long long blocks = (total + 255) / 256;
+    if (blocks > num_sms * 16) blocks = num_sms * 16;
+    if (blocks < 1) blocks = 1;
+    if (dtype == MOE_F32)
+        combine_kernel<float><<<(int)blocks, 256, 0, st>>>((const float*)x, (const float*)Ys,
+                                                           drop_mask, (const float*)Sh, (float*)y,
+                                                           T, d, k);
+    else
+        combine_kernel<__nv_bfloat16><<<(int)blocks, 256, 0, st>>>(
+            (const __nv_bfloat16*)x, (const __nv_bfloat16*)Ys, drop_mask,
+            (const __nv_bfloat16*)Sh, (__nv_bfloat16*)y, T, d, k);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

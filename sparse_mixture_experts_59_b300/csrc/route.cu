@@ -1,0 +1,215 @@
+// route.cu -- router GEMM and the softmax / top-k / renormalisation step.
+//
+// "How Mixture of Experts Works", section "The Gating Mechanism": a bias-free
+// linear router gives one logit per expert, softmax over all experts, top-k,
+// and the kept probabilities renormalised to sum to 1.  "Mixture of Experts
+// (MoE)", section "The router": scores = softmax(h @ W_r).  Ties in the top-k
+// go to the lower expert index; selection is on the fp32 logits (softmax is
+// monotone, so this is the same set without the ties that exp rounding can
+// create).  P_e (mean probability per expert) feeds the aux loss of "Load
+// balancing and expert collapse".
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace moe {
+
+// ----------------------------------------------------------------------------
+// logits[T,E] = x[T,d] . Wr[E,d]^T (+ bias[E]) on CUDA cores, fp32 accumulate.
+// 64x64 output tile per 256-thread block, 4x4 outputs per thread, K step 16.
+// Used for fp32 layers and for routers too narrow for a tensor-core tile.
+template <typename T>
+__global__ void __launch_bounds__(256)
+router_logits_simt(const T* __restrict__ x, const T* __restrict__ Wr,
+                   const float* __restrict__ bias, float* __restrict__ logits,
+                   int Ttok, int d, int E) {
+    constexpr int BM = 64, BN = 64, BK = 16;
+    __shared__ __align__(16) float Xs[BK][BM + 4];
+    __shared__ __align__(16) float Ws[BK][BN + 4];
+    const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+
+    for (int k0 = 0; k0 < d; k0 += BK) {
+        for (int i = threadIdx.x; i < BM * BK; i += 256) {
+            const int r = i / BK, c = i % BK;
+            const int gr = m0 + r, gc = k0 + c;
+            Xs[c][r] = (gr < Ttok && gc < d) ? Elem<T>::load(x + (size_t)gr * d + gc) : 0.f;
+            const int ge = n0 + r;
+            Ws[c][r] = (ge < E && gc < d) ? Elem<T>::load(Wr + (size_t)ge * d + gc) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < BK; ++kk) {
+            const float4 a = *reinterpret_cast<const float4*>(&Xs[kk][ty * 4]);
+            const float4 b = *reinterpret_cast<const float4*>(&Ws[kk][tx * 4]);
+            const float av[4] = {a.x, a.y, a.z, a.w};
+            const float bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int t = m0 + ty * 4 + i;
+        if (t >= Ttok) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int e = n0 + tx * 4 + j;
+            if (e < E) logits[(size_t)t * E + e] = acc[i][j] + (bias ? bias[e] : 0.f);
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------
+// Softmax / top-k / renormalise: one warp per token, each lane holding the
+// logits of experts lane, lane+32, ... (up to 8 per lane, E <= 256).
+// Per-block sums of p[t,e] go to prob_part[block][e]; the last block to finish
+// adds the partials in block order (deterministic) into prob_mean[e] / T.
+template <int VPL>
+__global__ void __launch_bounds__(256)
+router_topk_kernel(const float* __restrict__ logits, int Ttok, int E, int k,
+                   int* __restrict__ topk_idx, float* __restrict__ topk_w,
+                   float* __restrict__ prob_part, float* __restrict__ prob_mean,
+                   int* __restrict__ done_counter) {
+    constexpr int WARPS = 8;
+    __shared__ float s_psum[WARPS][kMaxExperts];
+    __shared__ int s_last;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool want_p = prob_mean != nullptr;
+    if (want_p)
+        for (int e = lane; e < E; e += 32) s_psum[warp][e] = 0.f;
+
+    for (int t = blockIdx.x * WARPS + warp; t < Ttok; t += gridDim.x * WARPS) {
+        float l[VPL];
+#pragma unroll
+        for (int j = 0; j < VPL; ++j) {
+            const int e = lane + 32 * j;
+            l[j] = (e < E) ? logits[(size_t)t * E + e] : -INFINITY;
+        }
+        float m = l[0];
+#pragma unroll
+        for (int j = 1; j < VPL; ++j) m = fmaxf(m, l[j]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float ex[VPL];
+        float z = 0.f;
+#pragma unroll
+        for (int j = 0; j < VPL; ++j) {
+            ex[j] = (lane + 32 * j < E) ? expf(l[j] - m) : 0.f;
+            z += ex[j];
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+        if (want_p) {
+            const float inv = 1.f / z;
+#pragma unroll
+            for (int j = 0; j < VPL; ++j)
+                if (lane + 32 * j < E) s_psum[warp][lane + 32 * j] += ex[j] * inv;
+        }
+        // top-k by repeated warp arg-max over the logits; (value desc, index asc)
+        unsigned taken = 0;       // bit j: lane's value j already selected
+        float kept_ex = 0.f, my_ex = 0.f;
+        int my_idx = -1;
+        for (int s = 0; s < k; ++s) {
+            float bv = -INFINITY;
+            int bi = 0x7fffffff;
+#pragma unroll
+            for (int j = 0; j < VPL; ++j) {
+                const int e = lane + 32 * j;
+                if (e < E && !(taken & (1u << j)) && (l[j] > bv || bi == 0x7fffffff)) {
+                    bv = l[j];
+                    bi = e;
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+            }
+            // owner marks it; everyone learns exp(l - m) of the winner
+            const int owner = bi & 31, jj = bi >> 5;
+            float wex = 0.f;
+#pragma unroll
+            for (int j = 0; j < VPL; ++j)
+                if (j == jj) wex = ex[j];
+            wex = __shfl_sync(0xffffffffu, wex, owner);
+            if (lane == owner) taken |= 1u << jj;
+            kept_ex += wex;
+            if (lane == s) { my_idx = bi; my_ex = wex; }
+        }
+        if (lane < k) {
+            topk_idx[(size_t)t * k + lane] = my_idx;
+            topk_w[(size_t)t * k + lane] = my_ex / kept_ex;
+        }
+    }
+    if (!want_p) return;
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < WARPS; ++w) s += s_psum[w][e];
+        prob_part[(size_t)blockIdx.x * E + e] = s;
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = (atomicAdd(done_counter, 1) == (int)gridDim.x - 1);
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        float s = 0.f;
+        for (int b = 0; b < (int)gridDim.x; ++b) s += __ldcg(prob_part + (size_t)b * E + e);
+        prob_mean[e] = s / (float)Ttok;
+    }
+    if (threadIdx.x == 0) *done_counter = 0;   // leave the workspace reusable
+}
+
+// ---------------------------------------------------------------- launchers
+cudaError_t launch_router_logits_simt(int dtype, const void* x, const void* Wr, const float* bias,
+                                      float* logits, int T, int d, int E, cudaStream_t st) {
+    dim3 grid((T + 63) / 64, (E + 63) / 64);
+    if (dtype == MOE_F32)
+        router_logits_simt<float><<<grid, 256, 0, st>>>((const float*)x, (const float*)Wr, bias,
+                                                        logits, T, d, E);
+    else
+        router_logits_simt<__nv_bfloat16><<<grid, 256, 0, st>>>(
+            (const __nv_bfloat16*)x, (const __nv_bfloat16*)Wr, bias, logits, T, d, E);
+    return cudaGetLastError();
+}
+
+int router_topk_blocks(int T, int num_sms) {
+    int b = (T + 7) / 8;
+    const int cap = num_sms * 4;
+    return b < cap ? (b > 0 ? b : 1) : cap;
+}
+
+cudaError_t launch_router_topk(const float* logits, int T, int E, int k, int* topk_idx,
+                               float* topk_w, float* prob_part, float* prob_mean, int* done,
+                               int nblocks, cudaStream_t st) {
+    const int vpl = (E + 31) / 32;
+#define MOE_TOPK_CASE(V)                                                                  \
+    case V:                                                                               \
+        router_topk_kernel<V><<<nblocks, 256, 0, st>>>(logits, T, E, k, topk_idx, topk_w,  \
+                                                       prob_part, prob_mean, done);       \
+        break;
+    switch (vpl) {
+        MOE_TOPK_CASE(1)
+        MOE_TOPK_CASE(2)
+        MOE_TOPK_CASE(4)
+        MOE_TOPK_CASE(8)
+        case 3: router_topk_kernel<4><<<nblocks, 256, 0, st>>>(logits, T, E, k, topk_idx, topk_w, prob_part, prob_mean, done); break;
+        default: router_topk_kernel<8><<<nblocks, 256, 0, st>>>(logits, T, E, k, topk_idx, topk_w, prob_part, prob_mean, done); break;
+    }
+#undef MOE_TOPK_CASE
+    return cudaGetLastError();
+}
+
+}  // namespace moe

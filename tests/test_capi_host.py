@@ -1,0 +1,101 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every
+function include/moe.h declares, and rejects bad arguments before it touches
+the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from sparse_mixture_experts_59_b300 import binding, build, workloads
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.lib()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_stage_calls():
+    names = _declared()
+    for n in ("moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_layer_forward",
+              "moe_workspace_size", "moe_workspace_init", "moe_get_device_status"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+    assert set(_declared()) <= set(binding.EXPORTS) | {"moe_status_string", "moe_last_error"}
+
+
+def test_status_strings(lib):
+    assert lib.moe_status_string(0) == b"MOE_OK"
+    assert lib.moe_status_string(6) == b"MOE_ERR_DEVICE_BOUNDS"
+
+
+def test_capacity_matches_formula(lib):
+    assert binding.capacity(workloads.config("tiny_fp32")) == 20
+    assert binding.capacity(workloads.config("switch_skewed")) == 256
+    assert binding.capacity(workloads.config("mixtral_prefill")) == -1
+    assert binding.capacity(dict(T=1, d=8, F=8, E=8, k=1, capacity_factor=0.5)) == 1
+
+
+def test_workspace_size_grows_with_tokens(lib):
+    a = binding.workspace_size(workloads.config("mixtral_prefill", T=64))
+    b = binding.workspace_size(workloads.config("mixtral_prefill", T=128))
+    assert 0 < a < b
+    # the gathered rows, hidden rows and slot outputs dominate
+    c = workloads.config("mixtral_prefill")
+    A = c["T"] * c["k"]
+    assert binding.workspace_size(c) >= A * (2 * c["d"] + c["F"]) * 2
+
+
+@pytest.mark.parametrize("bad,code", [
+    (dict(d=12), 1), (dict(F=0), 1), (dict(E=0), 1), (dict(E=300), 1), (dict(k=0), 1),
+    (dict(k=9, E=16), 1), (dict(k=3, E=2), 1), (dict(T=-1), 1), (dict(F_shared=4), 1),
+    (dict(act="swiglu", has_bias=True), 2), (dict(act="gelu", F_shared=64), 2),
+])
+def test_invalid_configs_are_rejected(lib, bad, code):
+    cfg = workloads.config("mixtral_prefill", T=16, d=64, F=64)
+    cfg.update(bad)
+    with pytest.raises(binding.MoeError) as ei:
+        binding.workspace_size(cfg)
+    assert ei.value.code == code
+
+
+def test_calls_check_arguments_before_launching(lib):
+    """NULL or misaligned pointers and a short workspace come back as error
+    codes from the host side (no device is touched: this runs without a GPU)."""
+    c = binding.make_config(workloads.config("mixtral_prefill", T=16, d=64, F=64))
+    need = binding.workspace_size(c)
+    fake = ctypes.c_void_p(1 << 40)        # never dereferenced: checks fail first
+    mis = ctypes.c_void_p((1 << 40) + 8)
+    P = ctypes.c_void_p
+    L = lib
+    assert L.moe_route(ctypes.byref(c), None, fake, None, fake, fake, fake, None, fake, need, None) == 1
+    assert L.moe_route(ctypes.byref(c), mis, fake, None, fake, fake, fake, None, fake, need, None) == 1
+    assert L.moe_route(ctypes.byref(c), fake, fake, None, fake, fake, fake, None, fake, need - 1, None) == 3
+    assert L.moe_route(ctypes.byref(c), fake, fake, None, fake, fake, fake, None, None, need, None) == 1
+    w = binding.MoeWeights(W1=fake.value, W3=None, W2=fake.value)
+    assert L.moe_expert_ffn(ctypes.byref(c), fake, fake, fake, fake, ctypes.byref(w), fake, None,
+                            fake, need, None) == 1          # W3 missing for SwiGLU
+    assert b"W3" in L.moe_last_error()
+    assert L.moe_combine(ctypes.byref(c), fake, fake, None, None, fake, None) == 1
+    out = binding.MoeLayerOut(y=None)
+    w = binding.MoeWeights(W1=fake.value, W3=fake.value, W2=fake.value)
+    assert L.moe_layer_forward(ctypes.byref(c), fake, fake, None, ctypes.byref(w), ctypes.byref(out),
+                               fake, need, None) == 1       # y missing
+    # T = 0 is a no-op that succeeds without touching anything
+    z = binding.make_config(workloads.config("mixtral_prefill", T=0, d=64, F=64))
+    nz = binding.workspace_size(z)
+    assert L.moe_route(ctypes.byref(z), None, None, None, None, None, None, None, fake, nz, None) == 0
+    assert L.moe_combine(ctypes.byref(z), None, None, None, None, None, None) == 0

@@ -1,0 +1,118 @@
+"""GPU edge cases: tiny and ragged token counts, one expert, k = E, an
+all-ties router, capacity 1, dispatch over many look-back blocks, and bad
+expert indices (reported as a device status; the context stays usable)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import TOL_Y, f64, max_rel
+from sparse_mixture_experts_59_b300 import binding, workloads
+
+pytestmark = pytest.mark.gpu
+
+
+def _layer_vs_oracle(cfg, zero_router=False):
+    inp_cpu = workloads.make_inputs(cfg, device="cpu")
+    if zero_router:
+        inp_cpu["Wr"] = torch.zeros_like(inp_cpu["Wr"])
+    inp = workloads.to_device(inp_cpu, "cuda")
+    layer = binding.MoeLayer(cfg, inp)
+    out = layer.forward(inp["x"], want=("logits", "topk_idx", "drop_mask", "stats", "counts_kept"))
+    torch.cuda.synchronize()
+    assert binding.device_status(layer.ws) == 0
+    ref = oracle.layer_forward(inp_cpu, logits_in=f64(out["logits"]))
+    np.testing.assert_array_equal(out["topk_idx"].cpu().numpy(), ref["topk_idx"])
+    np.testing.assert_array_equal(out["drop_mask"].cpu().numpy(), ref["drop_mask"])
+    np.testing.assert_array_equal(out["counts_kept"].cpu().numpy(), ref["counts_kept"])
+    assert max_rel(f64(out["y"]), ref["y"]) < TOL_Y[cfg["dtype"]]
+    assert max_rel(f64(out["y"]) - f64(inp_cpu["x"]), ref["y"] - f64(inp_cpu["x"])) < TOL_Y[cfg["dtype"]]
+    return out, ref
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("T", [1, 7, 129])
+def test_small_and_ragged_token_counts(T, dtype):
+    cfg = workloads.config("mixtral_prefill", T=T, d=136, F=200, E=8, k=2, dtype=dtype, seed=3000 + T)
+    _layer_vs_oracle(cfg)
+
+
+@pytest.mark.parametrize("act", ["swiglu", "gelu"])
+def test_single_expert_is_dense_ffn(act):
+    cfg = workloads.config("switch_skewed" if act == "gelu" else "mixtral_prefill", T=150, d=128,
+                           F=256, E=1, k=1, capacity_factor=0.0, skew=False, seed=3100)
+    out, ref = _layer_vs_oracle(cfg)
+    assert np.all(out["topk_idx"].cpu().numpy() == 0)
+
+
+def test_k_equals_E():
+    cfg = workloads.config("mixtral_prefill", T=64, d=128, F=128, E=4, k=4, seed=3200)
+    _layer_vs_oracle(cfg)
+
+
+@pytest.mark.parametrize("cf", [0.0, 1.0, 0.3])
+def test_all_ties_router_takes_lowest_experts(cf):
+    """Wr = 0: every token picks experts 0..k-1, aux = k, and with a capacity
+    the tokens past it keep y = x."""
+    cfg = workloads.config("tiny_fp32", T=200, E=8, k=2, dtype="bf16", capacity_factor=cf, seed=3300)
+    out, ref = _layer_vs_oracle(cfg, zero_router=True)
+    assert np.all(out["topk_idx"].cpu().numpy() == np.arange(2)[None, :])
+    assert float(out["stats"][0]) == pytest.approx(2.0, rel=1e-6)
+
+
+def test_capacity_one():
+    cfg = workloads.config("switch_skewed", T=100, d=64, F=128, E=64, k=1, capacity_factor=0.01,
+                           seed=3400)
+    out, ref = _layer_vs_oracle(cfg)
+    assert ref["cap"] == 1
+    assert int(out["counts_kept"].max()) <= 1
+
+
+@pytest.mark.parametrize("A,E,k,cap", [(70001 * 1, 64, 1, -1), (40000 * 2, 256, 2, 300),
+                                       (2049, 3, 1, 100), (65536, 256, 8, -1)])
+def test_dispatch_many_blocks(A, E, k, cap):
+    """Dispatch over many decoupled look-back blocks, with skewed expert
+    choices, against the oracle bit for bit."""
+    T = A // k
+    g = np.random.default_rng(A + E)
+    # Zipf-like skew: low expert ids much more frequent; distinct per token
+    p = 1.0 / np.arange(1, E + 1) ** 1.1
+    p /= p.sum()
+    idx = np.stack([g.choice(E, size=k, replace=False, p=p) for _ in range(T)]).astype(np.int32)
+    cf = 0.0 if cap < 0 else cap * E / (T * k) + 1e-9
+    cfg = workloads.config("mixtral_prefill", T=T, d=64, F=64, E=E, k=k, capacity_factor=cf)
+    c = binding.make_config(cfg)
+    want_cap = binding.capacity(c)
+    ref = oracle.dispatch(idx, E, want_cap)
+    do = binding.dispatch(c, torch.from_numpy(idx).cuda())
+    torch.cuda.synchronize()
+    for key in ("counts_pre", "counts_kept", "offsets", "dest", "drop_mask"):
+        np.testing.assert_array_equal(do[key].cpu().numpy()[:len(ref[key])], ref[key], err_msg=key)
+    np.testing.assert_array_equal(do["perm_src"].cpu().numpy()[:ref["R"]], ref["perm_src"])
+    # again on the same workspace (the look-back state must have been cleared)
+    ws = binding.new_workspace(c)
+    for _ in range(2):
+        do = binding.dispatch(c, torch.from_numpy(idx).cuda(), ws=ws)
+        np.testing.assert_array_equal(do["dest"].cpu().numpy(), ref["dest"])
+    assert binding.device_status(ws) == 0
+
+
+def test_out_of_range_expert_index_is_reported():
+    """A corrupted top-k index is left out of every count and reported as
+    MOE_ERR_DEVICE_BOUNDS; the next call on a re-initialised workspace works."""
+    cfg = workloads.config("mixtral_prefill", T=300, d=64, F=64, E=8, k=2)
+    c = binding.make_config(cfg)
+    idx = torch.randint(0, 8, (300, 2), dtype=torch.int32)
+    idx[:, 1] = (idx[:, 0] + 1) % 8
+    bad = idx.clone()
+    bad[17, 0] = 8
+    bad[200, 1] = -3
+    ws = binding.new_workspace(c)
+    do = binding.dispatch(c, bad.cuda(), ws=ws)
+    assert binding.device_status(ws) == 6          # MOE_ERR_DEVICE_BOUNDS
+    assert int(do["counts_pre"].sum()) == 600 - 2
+    ws = binding.new_workspace(c)
+    do = binding.dispatch(c, idx.cuda(), ws=ws)
+    ref = oracle.dispatch(idx.numpy(), 8, -1)
+    np.testing.assert_array_equal(do["dest"].cpu().numpy(), ref["dest"])
+    assert binding.device_status(ws) == 0
