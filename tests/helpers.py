@@ -56,6 +56,21 @@ def max_rel(got, ref):
     return float(np.max(np.abs(got - ref)) / scale)
 
 
+def moe_rel(y, y_ref, x, dtype):
+    """Error of the MoE contribution y - x, relative to max|y_ref - x|, after
+    allowing each output element its own rounding to the output dtype (half a
+    bf16 ulp is at most 2^-8 |y|).  With x of order 1 and an MoE
+    contribution of order 0.05, that rounding alone would otherwise exceed the
+    tolerance, so the residual cannot hide an MoE error either way."""
+    y = np.asarray(y, np.float64)
+    y_ref = np.asarray(y_ref, np.float64)
+    x = np.asarray(x, np.float64)
+    slack = (2.0 ** -8) * np.abs(y_ref) if dtype == "bf16" else 0.0
+    excess = np.maximum(np.abs(y - y_ref) - slack, 0.0)
+    scale = np.max(np.abs(y_ref - x)) if y_ref.size else 0.0
+    return float(np.max(excess) / scale) if scale > 0 else float(np.max(excess, initial=0.0))
+
+
 def f64(t):
     return t.detach().double().cpu().numpy() if isinstance(t, torch.Tensor) else np.asarray(t, np.float64)
 
