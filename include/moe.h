@@ -213,6 +213,31 @@ int moe_layer_forward_profiled(const moe_cfg *cfg, const void *x, const void *Wr
                                const moe_layer_out *out, void *ws, size_t ws_bytes, void *stream,
                                void *const *events);
 
+/* moe_dispatch for callers that cannot allocate device memory.  (The pages
+ * have no counterpart; this is a deployment variant of moe_dispatch.)
+ * moe_dispatch needs a caller-allocated workspace for its scratch.  Some
+ * callers cannot call cudaMalloc or hand over extra device memory -- e.g. a
+ * host framework that owns every allocation and passes an operator only its
+ * inputs and outputs.  This variant takes the same inputs and outputs as
+ * moe_dispatch (no workspace) and keeps its scratch in a fixed device array
+ * inside the library (294,912 bytes per GPU that loads the library, held
+ * until the process exits); it allocates nothing.
+ *  - T*k must be <= 65536; larger calls return MOE_ERR_INVALID_ARG and launch
+ *    nothing.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - Every call clears the scratch's control words, then uses it; all calls
+ *    in the process share the one array, so calls that overlap on the GPU
+ *    (other streams, other threads) race and must be serialised by the caller.
+ *  - device_status (optional, device int): receives the call's device status
+ *    (MOE_OK or MOE_ERR_DEVICE_*) on `stream`, in place of moe_get_device_status.
+ * Outputs and their meaning are those of moe_dispatch. */
+int moe_dispatch_noalloc(const moe_cfg *cfg, const int *topk_idx, const float *prob_mean,
+                         int *counts_pre, int *counts_kept, int *offsets, int *perm_src,
+                         int *dest, unsigned char *drop_mask, float *stats, int *device_status,
+                         void *stream);
+
 /* Reads (and leaves) the device status word of a workspace: MOE_OK, or the
  * first MOE_ERR_DEVICE_* recorded since the last init.  Synchronises `stream`. */
 int moe_get_device_status(void *ws, size_t ws_bytes, void *stream, int *status);

@@ -20,7 +20,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
           7: "MOE_ERR_NO_DEVICE"}
 EXPORTS = ("moe_status_string", "moe_last_error", "moe_capacity", "moe_workspace_size",
            "moe_workspace_init", "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine",
-           "moe_layer_forward", "moe_layer_forward_profiled", "moe_get_device_status")
+           "moe_layer_forward", "moe_layer_forward_profiled", "moe_get_device_status",
+           "moe_dispatch_noalloc")
 
 
 class MoeError(RuntimeError):
@@ -73,6 +74,7 @@ def lib():
         L.moe_layer_forward.argtypes = [P, P, P, P, P, P, P, S, P]
         L.moe_layer_forward_profiled.argtypes = [P, P, P, P, P, P, P, S, P, P]
         L.moe_get_device_status.argtypes = [P, S, P, ctypes.POINTER(I)]
+        L.moe_dispatch_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P]
         for name in EXPORTS:
             getattr(L, name).restype = getattr(L, name).restype or I
         _lib = L
@@ -165,6 +167,29 @@ def dispatch(cfg, topk_idx, prob_mean=None, ws=None, stream=None):
                               _p(out["dest"]), _p(out["drop_mask"]),
                               _p(out["stats"]) if prob_mean is not None else None,
                               _p(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def dispatch_noalloc(cfg, topk_idx, prob_mean=None, stream=None):
+    """moe_dispatch_noalloc: the outputs of dispatch() plus device_status [1]
+    int32, with no workspace (the library's fixed scratch array is used;
+    T*k <= 65536)."""
+    c = cfg if isinstance(cfg, MoeConfig) else make_config(cfg)
+    dev = topk_idx.device
+    A = c.T * c.k
+    i32 = dict(dtype=torch.int32, device=dev)
+    out = dict(counts_pre=torch.empty(c.E, **i32), counts_kept=torch.empty(c.E, **i32),
+               offsets=torch.empty(c.E + 1, **i32), perm_src=torch.full((max(A, 1),), -1, **i32),
+               dest=torch.empty(max(A, 1), **i32),
+               drop_mask=torch.empty(max(A, 1), dtype=torch.uint8, device=dev),
+               stats=torch.zeros(2, dtype=torch.float32, device=dev),
+               device_status=torch.full((1,), -1, **i32))
+    _check(lib().moe_dispatch_noalloc(ctypes.byref(c), _p(topk_idx), _p(prob_mean),
+                                      _p(out["counts_pre"]), _p(out["counts_kept"]),
+                                      _p(out["offsets"]), _p(out["perm_src"]), _p(out["dest"]),
+                                      _p(out["drop_mask"]),
+                                      _p(out["stats"]) if prob_mean is not None else None,
+                                      _p(out["device_status"]), _stream(stream)))
     return out
 
 

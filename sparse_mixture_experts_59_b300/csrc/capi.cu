@@ -315,6 +315,12 @@ int run_expert_ffn(const moe_cfg& c, const DevInfo& di, const void* x, const int
 
 }  // namespace
 
+// Error reporting for the other host translation units of the library.
+namespace moe {
+int set_last_error(int code, const char* msg) { return fail(code, "%s", msg); }
+int set_cuda_error(cudaError_t e, const char* where) { return fail_cuda(e, where); }
+}  // namespace moe
+
 // ====================================================================== ABI
 extern "C" {
 

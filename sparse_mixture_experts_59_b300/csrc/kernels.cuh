@@ -16,6 +16,10 @@ constexpr int kDspItems = 8;
 constexpr int kDspChunk = 256 * kDspItems;
 inline int dispatch_blocks(int A) { return A > 0 ? (A + kDspChunk - 1) / kDspChunk : 1; }
 
+// capi.cu: record a host-side failure for moe_last_error and return `code`
+int set_last_error(int code, const char* msg);
+int set_cuda_error(cudaError_t e, const char* where);   // returns MOE_ERR_CUDA
+
 // route.cu
 cudaError_t launch_router_logits_simt(int dtype, const void* x, const void* Wr, const float* bias,
                                       float* logits, int T, int d, int E, cudaStream_t st);
