@@ -44,6 +44,8 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="mixtral_prefill")
     ap.add_argument("--decode-workload", default="mixtral_decode")
+    ap.add_argument("--tokens", type=int, default=None, help="override T (profiling cases)")
+    ap.add_argument("--experts", type=int, default=None, help="override E (profiling cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
@@ -201,10 +203,19 @@ def time_layer(layer, x, steps, warmup, world, outputs, clocks=None):
     return ms, {n: float(stages[:, j].mean()) for j, n in enumerate(names)}, clk
 
 
+def workload_config(args):
+    over = {}
+    if args.tokens is not None:
+        over["T"] = args.tokens
+    if args.experts is not None:
+        over["E"] = args.experts
+    return workloads.config(args.workload, **over)
+
+
 def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     peaks, peak_src = measured_peaks()
-    cfg = workloads.config(args.workload)
+    cfg = workload_config(args)
     inp = workloads.make_inputs(cfg, device=dev)
     layer = binding.MoeLayer(cfg, inp, device=dev)
     x = inp["x"]
@@ -359,7 +370,7 @@ def cpu_baseline(inp, cfg, seconds):
 def run_reference(args, world, rank, local):
     """The CPU oracle as the baseline arm, timed on the host cores."""
     import oracle
-    cfg = workloads.config(args.workload)
+    cfg = workload_config(args)
     dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
     inp_cpu = _host_inputs(workloads.make_inputs(cfg, device=dev))
     if dev.type == "cuda":

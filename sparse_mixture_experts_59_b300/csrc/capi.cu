@@ -38,8 +38,9 @@ int router_blocks(int T) {
 }
 
 struct Layout {
-    size_t ctrl, tile_status, rank, prob_part, prob_mean, logits, topk_idx, topk_w, counts_pre,
-        counts_kept, offsets, perm_src, dest, drop_mask, stats, xp, h, hsh, ys, sh, total;
+    size_t ctrl, tile_status, rank, prob_part, prob_mean, router_part, logits, topk_idx, topk_w,
+        counts_pre, counts_kept, offsets, perm_src, dest, drop_mask, stats, xp, h, hsh, ys, sh,
+        total;
 };
 
 Layout layout_of(const moe_cfg& c) {
@@ -52,6 +53,9 @@ Layout layout_of(const moe_cfg& c) {
     L.rank = take(A * 4);
     L.prob_part = take((size_t)router_blocks(c.T) * E * 4);
     L.prob_mean = take(E * 4);
+    L.router_part = take(c.dtype == MOE_BF16
+                             ? (size_t)router_tc_plan(c.T > 0 ? c.T : 1, c.d, c.E).splits * T * E * 4
+                             : 0);
     L.logits = take(T * E * 4);
     L.topk_idx = take(A * 4);
     L.topk_w = take(A * 4);
@@ -180,15 +184,16 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// bf16 row-major [rows, cols] matrix; box = 128 rows x 64 columns (128 bytes),
-// 128-byte swizzle, out-of-range elements read as zero.
-int encode_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, const char* what) {
+// bf16 row-major [rows, cols] matrix; box = box_rows rows x 64 columns (128
+// bytes), 128-byte swizzle, out-of-range elements read as zero.
+int encode_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, const char* what,
+                uint32_t box_rows = 128) {
     auto fn = encode_fn();
     if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled unavailable%s");
     if (rows == 0) rows = 1;
     const cuuint64_t dims[2] = {cols, rows};
     const cuuint64_t strides[1] = {cols * 2};
-    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t box[2] = {64, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -206,13 +211,30 @@ int run_route(const moe_cfg& c, const DevInfo& di, const void* x, const void* Wr
               const float* bias, float* logits, int* topk_idx, float* topk_w, float* prob_mean,
               void* ws, cudaStream_t st) {
     const Layout L = layout_of(c);
-    MOE_CUDA(launch_router_logits_simt(c.dtype, x, Wr, bias, logits, c.T, c.d, c.E, st),
-             "router logits launch");
-    MOE_CUDA(launch_router_topk(logits, c.T, c.E, c.k, topk_idx, topk_w, at<float>(ws, L.prob_part),
-                                prob_mean, at<int>(ws, L.ctrl) + kCtrlRouterDone,
-                                router_blocks(c.T), st),
+    const float* part = logits;
+    int nsplit = 1;
+    const float* topk_bias = nullptr;
+    if (c.dtype == MOE_BF16) {
+        if (di.cc != 103)
+            return fail(MOE_ERR_UNSUPPORTED, "the bf16 router needs an sm_103a (B300) device%s");
+        const RouterPlan plan = router_tc_plan(c.T, c.d, c.E);
+        CUtensorMap mx, mw;
+        MOE_TRY(encode_rows(&mx, x, (uint64_t)c.T, c.d, "x", 128));
+        MOE_TRY(encode_rows(&mw, Wr, (uint64_t)c.E, c.d, "Wr", (uint32_t)plan.NB));
+        float* rp = at<float>(ws, L.router_part);
+        MOE_CUDA(launch_router_tc(mx, mw, c.T, c.E, plan, rp, at<int>(ws, L.ctrl) + kCtrlStatus, st),
+                 "router GEMM launch");
+        part = rp;
+        nsplit = plan.splits;
+        topk_bias = bias;
+    } else {
+        MOE_CUDA(launch_router_logits_simt(c.dtype, x, Wr, bias, logits, c.T, c.d, c.E, st),
+                 "router logits launch");
+    }
+    MOE_CUDA(launch_router_topk(part, nsplit, topk_bias, logits, c.T, c.E, c.k, topk_idx, topk_w,
+                                at<float>(ws, L.prob_part), prob_mean,
+                                at<int>(ws, L.ctrl) + kCtrlRouterDone, router_blocks(c.T), st),
              "router top-k launch");
-    (void)di;
     return MOE_OK;
 }
 

@@ -23,10 +23,23 @@ int set_cuda_error(cudaError_t e, const char* where);   // returns MOE_ERR_CUDA
 // route.cu
 cudaError_t launch_router_logits_simt(int dtype, const void* x, const void* Wr, const float* bias,
                                       float* logits, int T, int d, int E, cudaStream_t st);
-int router_topk_blocks(int T, int num_sms);
-cudaError_t launch_router_topk(const float* logits, int T, int E, int k, int* topk_idx,
-                               float* topk_w, float* prob_part, float* prob_mean, int* done,
-                               int nblocks, cudaStream_t st);
+// top-k reads nsplit partial-logit slabs part[s][T][E], adds them in order
+// and the bias, writes logits, then softmax / top-k / renormalise.
+cudaError_t launch_router_topk(const float* part, int nsplit, const float* bias, float* logits,
+                               int T, int E, int k, int* topk_idx, float* topk_w,
+                               float* prob_part, float* prob_mean, int* done, int nblocks,
+                               cudaStream_t st);
+
+// router_tc.cu (bf16 router logits on tcgen05, split over K)
+struct RouterPlan {
+    int NB;             // E rounded up to 16 (MMA N)
+    int m_tiles, nkb;   // 128-token tiles, 64-wide K blocks
+    int splits, kb_per_split;
+    int smem;           // dynamic shared memory bytes
+};
+RouterPlan router_tc_plan(int T, int d, int E);
+cudaError_t launch_router_tc(const CUtensorMap& map_x, const CUtensorMap& map_w, int T, int E,
+                             const RouterPlan& p, float* part, int* status, cudaStream_t st);
 
 // dispatch.cu
 cudaError_t launch_dispatch(const int* topk_idx, int T, int k, int E, long long cap,

@@ -74,7 +74,8 @@ router_logits_simt(const T* __restrict__ x, const T* __restrict__ Wr,
 // adds the partials in block order (deterministic) into prob_mean[e] / T.
 template <int VPL>
 __global__ void __launch_bounds__(256)
-router_topk_kernel(const float* __restrict__ logits, int Ttok, int E, int k,
+router_topk_kernel(const float* part, int nsplit, const float* __restrict__ bias,
+                   float* logits, int Ttok, int E, int k,
                    int* __restrict__ topk_idx, float* __restrict__ topk_w,
                    float* __restrict__ prob_part, float* __restrict__ prob_mean,
                    int* __restrict__ done_counter) {
@@ -88,10 +89,19 @@ router_topk_kernel(const float* __restrict__ logits, int Ttok, int E, int k,
 
     for (int t = blockIdx.x * WARPS + warp; t < Ttok; t += gridDim.x * WARPS) {
         float l[VPL];
+        const bool write_logits = (nsplit > 1) || (bias != nullptr) || (part != logits);
 #pragma unroll
         for (int j = 0; j < VPL; ++j) {
             const int e = lane + 32 * j;
-            l[j] = (e < E) ? logits[(size_t)t * E + e] : -INFINITY;
+            if (e < E) {
+                float v = part[(size_t)t * E + e];
+                for (int sp = 1; sp < nsplit; ++sp) v += part[((size_t)sp * Ttok + t) * E + e];
+                if (bias) v += bias[e];
+                if (write_logits) logits[(size_t)t * E + e] = v;
+                l[j] = v;
+            } else {
+                l[j] = -INFINITY;
+            }
         }
         float m = l[0];
 #pragma unroll
@@ -185,28 +195,32 @@ cudaError_t launch_router_logits_simt(int dtype, const void* x, const void* Wr, 
     return cudaGetLastError();
 }
 
-int router_topk_blocks(int T, int num_sms) {
-    int b = (T + 7) / 8;
-    const int cap = num_sms * 4;
-    return b < cap ? (b > 0 ? b : 1) : cap;
-}
-
-cudaError_t launch_router_topk(const float* logits, int T, int E, int k, int* topk_idx,
-                               float* topk_w, float* prob_part, float* prob_mean, int* done,
-                               int nblocks, cudaStream_t st) {
+cudaError_t launch_router_topk(const float* part, int nsplit, const float* bias, float* logits,
+                               int T, int E, int k, int* topk_idx, float* topk_w,
+                               float* prob_part, float* prob_mean, int* done, int nblocks,
+                               cudaStream_t st) {
     const int vpl = (E + 31) / 32;
 #define MOE_TOPK_CASE(V)                                                                  \
     case V:                                                                               \
-        router_topk_kernel<V><<<nblocks, 256, 0, st>>>(logits, T, E, k, topk_idx, topk_w,  \
-                                                       prob_part, prob_mean, done);       \
+        router_topk_kernel<V><<<nblocks, 256, 0, st>>>(part, nsplit, bias, logits, T, E, k,   \
+                                                       topk_idx, topk_w, prob_part,       \
+                                                       prob_mean, done);                  \
         break;
     switch (vpl) {
         MOE_TOPK_CASE(1)
         MOE_TOPK_CASE(2)
         MOE_TOPK_CASE(4)
         MOE_TOPK_CASE(8)
-        case 3: router_topk_kernel<4><<<nblocks, 256, 0, st>>>(logits, T, E, k, topk_idx, topk_w, prob_part, prob_mean, done); break;
-        default: router_topk_kernel<8><<<nblocks, 256, 0, st>>>(logits, T, E, k, topk_idx, topk_w, prob_part, prob_mean, done); break;
+        case 3:
+            router_topk_kernel<4><<<nblocks, 256, 0, st>>>(part, nsplit, bias, logits, T, E, k,
+                                                           topk_idx, topk_w, prob_part, prob_mean,
+                                                           done);
+            break;
+        default:
+            router_topk_kernel<8><<<nblocks, 256, 0, st>>>(part, nsplit, bias, logits, T, E, k,
+                                                           topk_idx, topk_w, prob_part, prob_mean,
+                                                           done);
+            break;
     }
 #undef MOE_TOPK_CASE
     return cudaGetLastError();
