@@ -5,6 +5,7 @@
 #include <math.h>
 #include <stdint.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <mutex>
@@ -203,6 +204,20 @@ int encode_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, 
     return MOE_OK;
 }
 
+// Kernel choice for the bf16 expert GEMMs: the 2-SM kernel (256-row tiles)
+// when the expert segments average at least 384 rows, so that partly filled
+// tiles waste little; else the 1-SM kernel (128-row tiles).  The environment
+// variable MOE_GEMM_PAIR=0 or 1 forces one of them.
+bool use_pair_kernel(const moe_cfg& c) {
+    const char* env = getenv("MOE_GEMM_PAIR");
+    if (env && env[0] == '0') return false;
+    if (env && env[0] == '1') return true;
+    long long rows = (long long)c.T * c.k;
+    const long long cap = moe_capacity(&c);
+    if (cap >= 0 && rows > cap * c.E) rows = cap * c.E;
+    return rows >= 384LL * c.E;
+}
+
 template <typename T>
 T* at(void* ws, size_t off) { return reinterpret_cast<T*>(static_cast<char*>(ws) + off); }
 
@@ -309,7 +324,10 @@ int run_expert_ffn(const moe_cfg& c, const DevInfo& di, const void* x, const int
     up.out = H; up.out_sh = Hsh;
     up.bias = c.has_bias ? (const __nv_bfloat16*)w.b1 : nullptr;
     up.status = status;
-    MOE_CUDA(launch_ffn_tc(c.act == MOE_SWIGLU ? kModeSwiglu : kModeGelu, maps, up, di.num_sms, st),
+    const bool pair = use_pair_kernel(c);
+    const int up_mode = c.act == MOE_SWIGLU ? kModeSwiglu : kModeGelu;
+    MOE_CUDA(pair ? launch_ffn_tc2(up_mode, maps, up, st)
+                  : launch_ffn_tc(up_mode, maps, up, di.num_sms, st),
              "up-projection launch");
     if (ev) MOE_CUDA(cudaEventRecord(ev[1], st), "event record");
     // down-projection maps
@@ -330,7 +348,9 @@ int run_expert_ffn(const moe_cfg& c, const DevInfo& di, const void* x, const int
     dn.bias = c.has_bias ? (const __nv_bfloat16*)w.b2 : nullptr;
     dn.perm_src = perm_src; dn.gate_w = topk_w;
     dn.status = status;
-    MOE_CUDA(launch_ffn_tc(kModeDown, maps, dn, di.num_sms, st), "down-projection launch");
+    MOE_CUDA(pair ? launch_ffn_tc2(kModeDown, maps, dn, st)
+                  : launch_ffn_tc(kModeDown, maps, dn, di.num_sms, st),
+             "down-projection launch");
     if (ev) MOE_CUDA(cudaEventRecord(ev[2], st), "event record");
     return MOE_OK;
 }

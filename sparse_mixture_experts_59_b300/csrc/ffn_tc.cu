@@ -30,14 +30,17 @@
 // tile reads (the next segment, or TMA's zero fill) and never stored.
 #include "common.cuh"
 #include "kernels.cuh"
+#include "ffn_tc_common.cuh"
 #include "tc_ptx.cuh"
 
 namespace moe {
 
 namespace {
 
+using tcffn::BK;
+using tcffn::ModeTraits;
+using tcffn::Tile;
 constexpr int BM = 128;        // tile rows = MMA M
-constexpr int BK = 64;         // bf16 elements per 128-byte swizzled row
 constexpr int MMA_N = 256;     // B rows per stage
 constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;        // 16 KB
@@ -57,64 +60,6 @@ constexpr int OFF_START = OFF_MISC + 16;                  // group tile starts
 constexpr int OFF_OFFS = OFF_START + (kMaxExperts + 2) * 4;  // cached offsets
 constexpr int SMEM_USED = OFF_OFFS + (kMaxExperts + 2) * 4;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;              // alignment slack
-
-template <int MODE> struct ModeTraits;
-template <> struct ModeTraits<kModeSwiglu> { static constexpr int BN_OUT = 128; };
-template <> struct ModeTraits<kModeGelu> { static constexpr int BN_OUT = 256; };
-template <> struct ModeTraits<kModeDown> { static constexpr int BN_OUT = 256; };
-
-struct Tile {
-    int g;          // group (E = shared expert)
-    bool sh;
-    int arow;       // first A row of the tile in its tensor map
-    int row_end;    // one past the segment's last A row
-    int n0;         // first output column
-    int wrow0, wrow1;  // weight rows of the two 128-row B boxes
-    int N, nk;
-};
-
-template <int MODE>
-__device__ __forceinline__ Tile decode_tile(const TcFfnArgs& p, const int* s_start,
-                                            const int* s_off, int G, int tile) {
-    constexpr int BN_OUT = ModeTraits<MODE>::BN_OUT;
-    Tile t;
-    t.g = find_group(s_start, G, tile);
-    t.sh = (t.g == p.E);
-    const int seg0 = t.sh ? 0 : s_off[t.g];
-    const int rows = t.sh ? p.rows_sh : s_off[t.g + 1] - seg0;
-    const int mt = (rows + BM - 1) / BM;
-    const int local = tile - s_start[t.g];
-    const int n = local / mt, m = local - (local / mt) * mt;
-    t.arow = seg0 + m * BM;
-    t.row_end = seg0 + rows;
-    t.N = t.sh ? p.N_sh : p.N;
-    const int K = t.sh ? p.K_sh : p.K;
-    t.nk = (K + BK - 1) / BK;
-    t.n0 = n * BN_OUT;
-    const int wbase = t.sh ? 0 : t.g * p.N;
-    if (MODE == kModeSwiglu) {
-        t.wrow0 = wbase + t.n0;      // gate rows (map B)
-        t.wrow1 = wbase + t.n0;      // up rows   (map B2)
-    } else {
-        t.wrow0 = wbase + t.n0;
-        t.wrow1 = wbase + t.n0 + 128;
-    }
-    return t;
-}
-
-__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const float (&v)[32], int ncols) {
-    // ncols = number of valid columns in this 32-wide chunk (multiple of 8)
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        if (q * 8 < ncols) {
-            uint4 pk = make_uint4(pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]),
-                                  pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]),
-                                  pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]),
-                                  pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]));
-            reinterpret_cast<uint4*>(dst)[q] = pk;
-        }
-    }
-}
 
 template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -178,7 +123,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
             int it = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-                const Tile t = decode_tile<MODE>(p, s_start, s_off, G, tile);
+                const Tile t = tcffn::decode_tile<MODE, BM>(p, s_start, s_off, G, tile);
                 const CUtensorMap* mA = t.sh ? &mapA_sh : &mapA;
                 const CUtensorMap* mB0 = t.sh ? &mapB_sh : &mapB;
                 const CUtensorMap* mB1 = (MODE == kModeSwiglu) ? (t.sh ? &mapB2_sh : &mapB2) : mB0;
@@ -206,7 +151,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
             int it = 0, tc = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++tc) {
-                const Tile t = decode_tile<MODE>(p, s_start, s_off, G, tile);
+                const Tile t = tcffn::decode_tile<MODE, BM>(p, s_start, s_off, G, tile);
                 const int acc = tc & 1;
                 const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
                 if (!ptx::mbar_wait(&tempty[acc], aph ^ 1u, s_abort)) { ok = false; break; }
@@ -242,7 +187,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
         const int row_in_tile = q * 32 + lane;
         int tc = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++tc) {
-            const Tile t = decode_tile<MODE>(p, s_start, s_off, G, tile);
+            const Tile t = tcffn::decode_tile<MODE, BM>(p, s_start, s_off, G, tile);
             const int acc = tc & 1;
             const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
             int ok = 1;
@@ -257,75 +202,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
             }
             ptx::tc_fence_after();
             const uint32_t taddr = tmem_base + (uint32_t)(acc * MMA_N) + ((uint32_t)(q * 32) << 16);
-            const int r = t.arow + row_in_tile;
-            const bool row_ok = r < t.row_end;
-
-            if (MODE == kModeSwiglu) {
-                __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(t.sh ? p.out_sh : p.out) +
-                                     (size_t)r * t.N + t.n0;
-#pragma unroll 1
-                for (int c = 0; c < BN_OUT; c += 32) {
-                    __syncwarp();
-                    float g[32], u[32];
-                    ptx::tmem_ld32(taddr + c, g);
-                    ptx::tmem_ld32(taddr + 128 + c, u);
-                    const int ncols = t.N - (t.n0 + c);
-                    if (row_ok && ncols > 0) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) g[j] = silu(g[j]) * u[j];
-                        store_row32(dst + c, g, ncols);
-                    }
-                }
-            } else if (MODE == kModeGelu) {
-                __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(t.sh ? p.out_sh : p.out) +
-                                     (size_t)r * t.N + t.n0;
-                const __nv_bfloat16* bias = (p.bias && !t.sh) ? p.bias + (size_t)t.g * t.N : nullptr;
-#pragma unroll 1
-                for (int c = 0; c < BN_OUT; c += 32) {
-                    __syncwarp();
-                    float v[32];
-                    ptx::tmem_ld32(taddr + c, v);
-                    const int ncols = t.N - (t.n0 + c);
-                    if (row_ok && ncols > 0) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const int n = t.n0 + c + j;
-                            const float b = (bias && n < t.N) ? __bfloat162float(bias[n]) : 0.f;
-                            v[j] = gelu_erf(v[j] + b);
-                        }
-                        store_row32(dst + c, v, ncols);
-                    }
-                }
-            } else {   // kModeDown
-                __nv_bfloat16* dst = nullptr;
-                float scale = 1.f;
-                if (row_ok) {
-                    if (t.sh) {
-                        dst = reinterpret_cast<__nv_bfloat16*>(p.out_sh) + (size_t)r * t.N + t.n0;
-                    } else {
-                        const int a = p.perm_src[r];
-                        scale = p.gate_w[a];
-                        dst = reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t)a * t.N + t.n0;
-                    }
-                }
-                const __nv_bfloat16* bias = (p.bias && !t.sh) ? p.bias + (size_t)t.g * t.N : nullptr;
-#pragma unroll 1
-                for (int c = 0; c < BN_OUT; c += 32) {
-                    __syncwarp();
-                    float v[32];
-                    ptx::tmem_ld32(taddr + c, v);
-                    const int ncols = t.N - (t.n0 + c);
-                    if (row_ok && ncols > 0) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const int n = t.n0 + c + j;
-                            const float b = (bias && n < t.N) ? __bfloat162float(bias[n]) : 0.f;
-                            v[j] = scale * (v[j] + b);
-                        }
-                        store_row32(dst + c, v, ncols);
-                    }
-                }
-            }
+            tcffn::epilogue_tile<MODE>(p, t, taddr, t.arow + row_in_tile);
             ptx::tc_fence_before();
             ptx::mbar_arrive(&tempty[acc]);
         }

@@ -93,5 +93,8 @@ int ffn_tc_smem_bytes();
 // maps: A, B, B2, A_sh, B_sh, B2_sh (see ffn_tc.cu)
 cudaError_t launch_ffn_tc(int mode, const CUtensorMap* maps, const TcFfnArgs& p, int num_sms,
                           cudaStream_t st);
+// ffn_tc2.cu: the same on CTA pairs (cta_group::2), 256-row tiles; same maps
+int ffn_tc2_tile_rows();
+cudaError_t launch_ffn_tc2(int mode, const CUtensorMap* maps, const TcFfnArgs& p, cudaStream_t st);
 
 }  // namespace moe

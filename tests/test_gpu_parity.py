@@ -1,6 +1,8 @@
 """GPU parity of the whole path against the CPU oracle, element by element, on
 scaled-down copies of each workload (sizes that span several tiles and leave
 ragged row, column and reduction tails).  Calls go through the C ABI."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -14,9 +16,31 @@ pytestmark = pytest.mark.gpu
 WANT = ("logits", "topk_idx", "topk_w", "counts_pre", "counts_kept", "drop_mask", "stats")
 
 
-@pytest.fixture(scope="module", params=list(SMALL))
+def _params():
+    """Each small workload with the library's own GEMM choice, and the bf16
+    ones again with the 2-SM (CTA-pair) kernels forced."""
+    out = list(SMALL)
+    out += [n + "@pair" for n in SMALL if small_cfg(n)["dtype"] == "bf16"]
+    return out
+
+
+@pytest.fixture(scope="module", params=_params())
 def run(request):
-    cfg = small_cfg(request.param)
+    name, _, mode = request.param.partition("@")
+    old = os.environ.get("MOE_GEMM_PAIR")
+    if mode == "pair":
+        os.environ["MOE_GEMM_PAIR"] = "1"
+    try:
+        yield _run(name)
+    finally:
+        if old is None:
+            os.environ.pop("MOE_GEMM_PAIR", None)
+        else:
+            os.environ["MOE_GEMM_PAIR"] = old
+
+
+def _run(name):
+    cfg = small_cfg(name)
     inp_cpu = workloads.make_inputs(cfg, device="cpu")
     inp = workloads.to_device(inp_cpu, "cuda")
     layer = binding.MoeLayer(cfg, inp)
