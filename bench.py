@@ -46,6 +46,8 @@ def parse_args():
     ap.add_argument("--decode-workload", default="mixtral_decode")
     ap.add_argument("--tokens", type=int, default=None, help="override T (profiling cases)")
     ap.add_argument("--experts", type=int, default=None, help="override E (profiling cases)")
+    ap.add_argument("--gemm", default=None, choices=["tc1", "pair", "swap"],
+                    help="force the expert GEMM kernel (default: the library's choice)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
@@ -248,8 +250,10 @@ def run_ours(args, world, rank, local):
                    "experts": cfg["E"], "top_k": cfg["k"], "act": cfg["act"],
                    "capacity": "dropless" if not cfg["capacity_factor"] else cfg["capacity_factor"],
                    "l2": "inputs larger than L2 (expert weights %.2f GB vs 126 MB L2); no flush"
-                         % (sum(inp[k].numel() * 2 for k in ("W1", "W3", "W2")) / 1e9),
-                   "parallelism": "replicas" if world > 1 else "single"},
+                         % (sum(inp[k].numel() * 2 for k in ("W1", "W3", "W2")
+                                if inp.get(k) is not None) / 1e9),
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "gemm_kernel": args.gemm or "auto"},
         "roofline": roof,
         "grouped_gemm": {"tflops": round(gg_tf, 1), "frac_of_peak": round(gg_tf / peak_tf, 4),
                          "peak": peak_tf, "up_ms": round(stages["up_gemm"], 4),
@@ -409,6 +413,8 @@ def run_reference(args, world, rank, local):
 
 def main():
     args = parse_args()
+    if args.gemm:
+        os.environ["MOE_GEMM_KERNEL"] = args.gemm
     world, rank, local = dist_init()
     if args.impl == "reference":
         if rank == 0:

@@ -204,18 +204,31 @@ int encode_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, 
     return MOE_OK;
 }
 
-// Kernel choice for the bf16 expert GEMMs: the 2-SM kernel (256-row tiles)
-// when the expert segments average at least 384 rows, so that partly filled
-// tiles waste little; else the 1-SM kernel (128-row tiles).  The environment
-// variable MOE_GEMM_PAIR=0 or 1 forces one of them.
-bool use_pair_kernel(const moe_cfg& c) {
-    const char* env = getenv("MOE_GEMM_PAIR");
-    if (env && env[0] == '0') return false;
-    if (env && env[0] == '1') return true;
-    long long rows = (long long)c.T * c.k;
+// Kernel for the bf16 expert GEMMs:
+//   kGemmTc1   1-SM kernel, tokens on M in 128-row tiles (ffn_tc.cu)
+//   kGemmPair  2-SM kernel, tokens on M in 256-row tiles (ffn_tc2.cu)
+//   kGemmSwap  2-SM kernel, weights on M and tokens on N (ffn_swap.cu): a
+//              segment's last tile shrinks to a multiple of 32 tokens
+// Automatic choice (from B300 measurements of the five workloads): segments
+// of at most 256 rows on average that fit one token tile (capacity-limited
+// layers) -> swap; long segments (>= 512 rows) -> swap; segments a little
+// over one 256-token tile, which swap would cover with a second tile that
+// re-streams the weights, and decode-sized segments -> tc1.  The environment
+// variable MOE_GEMM_KERNEL=tc1|pair|swap forces one (MOE_GEMM_PAIR=1: pair).
+enum GemmKernel { kGemmTc1, kGemmPair, kGemmSwap };
+GemmKernel choose_gemm(const moe_cfg& c) {
+    const char* env = getenv("MOE_GEMM_KERNEL");
+    if (env && !strcmp(env, "tc1")) return kGemmTc1;
+    if (env && !strcmp(env, "pair")) return kGemmPair;
+    if (env && !strcmp(env, "swap")) return kGemmSwap;
+    const char* pair = getenv("MOE_GEMM_PAIR");
+    if (pair && pair[0] == '1') return kGemmPair;
+    if (pair && pair[0] == '0') return kGemmTc1;
+    const long long rows = (long long)c.T * c.k;
     const long long cap = moe_capacity(&c);
-    if (cap >= 0 && rows > cap * c.E) rows = cap * c.E;
-    return rows >= 384LL * c.E;
+    if (cap >= 0 && cap <= 256 && rows >= 32LL * c.E) return kGemmSwap;   // one tile each
+    if (rows >= 512LL * c.E) return kGemmSwap;
+    return kGemmTc1;
 }
 
 template <typename T>
@@ -306,8 +319,54 @@ int run_expert_ffn(const moe_cfg& c, const DevInfo& di, const void* x, const int
     }
     if (di.cc != 103)
         return fail(MOE_ERR_UNSUPPORTED, "bf16 expert GEMMs need an sm_103a (B300) device%s");
-    // up-projection maps: A, B, B2, A_sh, B_sh, B2_sh
+    const GemmKernel gk = choose_gemm(c);
+    const int up_mode = c.act == MOE_SWIGLU ? kModeSwiglu : kModeGelu;
+    TcFfnArgs up{};
+    up.offsets = offsets; up.E = c.E; up.rows_sh = rows_sh;
+    up.N = c.F; up.K = c.d; up.N_sh = c.F_shared; up.K_sh = c.d;
+    up.out = H; up.out_sh = Hsh;
+    up.bias = c.has_bias ? (const __nv_bfloat16*)w.b1 : nullptr;
+    up.status = status;
+    TcFfnArgs dn{};
+    dn.offsets = offsets; dn.E = c.E; dn.rows_sh = rows_sh;
+    dn.N = c.d; dn.K = c.F; dn.N_sh = c.d; dn.K_sh = c.F_shared;
+    dn.out = Ys; dn.out_sh = Sh;
+    dn.bias = c.has_bias ? (const __nv_bfloat16*)w.b2 : nullptr;
+    dn.perm_src = perm_src; dn.gate_w = topk_w;
+    dn.status = status;
     CUtensorMap maps[6];
+    if (gk == kGemmSwap) {
+        // maps: W, W3, X (token rows), W_sh, W3_sh, X_sh
+        const uint32_t wb_up = (uint32_t)ffn_swap_weight_box_rows(up_mode);
+        MOE_TRY(encode_rows(&maps[0], w.W1, (uint64_t)c.E * c.F, c.d, "W1", wb_up));
+        MOE_TRY(encode_rows(&maps[1], c.act == MOE_SWIGLU ? w.W3 : w.W1, (uint64_t)c.E * c.F, c.d,
+                            "W3", wb_up));
+        MOE_TRY(encode_rows(&maps[2], Xp, (uint64_t)A, c.d, "gathered rows"));
+        if (rows_sh) {
+            MOE_TRY(encode_rows(&maps[3], w.S1, (uint64_t)c.F_shared, c.d, "S1", wb_up));
+            MOE_TRY(encode_rows(&maps[4], w.S3, (uint64_t)c.F_shared, c.d, "S3", wb_up));
+            MOE_TRY(encode_rows(&maps[5], x, (uint64_t)c.T, c.d, "x"));
+        } else {
+            maps[3] = maps[0]; maps[4] = maps[1]; maps[5] = maps[2];
+        }
+        MOE_CUDA(launch_ffn_swap(up_mode, maps, up, st), "up-projection launch");
+        if (ev) MOE_CUDA(cudaEventRecord(ev[1], st), "event record");
+        const uint32_t wb_dn = (uint32_t)ffn_swap_weight_box_rows(kModeDown);
+        MOE_TRY(encode_rows(&maps[0], w.W2, (uint64_t)c.E * c.d, c.F, "W2", wb_dn));
+        maps[1] = maps[0];
+        MOE_TRY(encode_rows(&maps[2], H, (uint64_t)A, c.F, "hidden rows"));
+        if (rows_sh) {
+            MOE_TRY(encode_rows(&maps[3], w.S2, (uint64_t)c.d, c.F_shared, "S2", wb_dn));
+            maps[4] = maps[3];
+            MOE_TRY(encode_rows(&maps[5], Hsh, (uint64_t)c.T, c.F_shared, "shared hidden rows"));
+        } else {
+            maps[3] = maps[0]; maps[4] = maps[1]; maps[5] = maps[2];
+        }
+        MOE_CUDA(launch_ffn_swap(kModeDown, maps, dn, st), "down-projection launch");
+        if (ev) MOE_CUDA(cudaEventRecord(ev[2], st), "event record");
+        return MOE_OK;
+    }
+    // tokens on M: maps A, B, B2, A_sh, B_sh, B2_sh
     MOE_TRY(encode_rows(&maps[0], Xp, (uint64_t)A, c.d, "gathered rows"));
     MOE_TRY(encode_rows(&maps[1], w.W1, (uint64_t)c.E * c.F, c.d, "W1"));
     MOE_TRY(encode_rows(&maps[2], c.act == MOE_SWIGLU ? w.W3 : w.W1, (uint64_t)c.E * c.F, c.d, "W3"));
@@ -318,19 +377,11 @@ int run_expert_ffn(const moe_cfg& c, const DevInfo& di, const void* x, const int
     } else {
         maps[3] = maps[0]; maps[4] = maps[1]; maps[5] = maps[2];
     }
-    TcFfnArgs up{};
-    up.offsets = offsets; up.E = c.E; up.rows_sh = rows_sh;
-    up.N = c.F; up.K = c.d; up.N_sh = c.F_shared; up.K_sh = c.d;
-    up.out = H; up.out_sh = Hsh;
-    up.bias = c.has_bias ? (const __nv_bfloat16*)w.b1 : nullptr;
-    up.status = status;
-    const bool pair = use_pair_kernel(c);
-    const int up_mode = c.act == MOE_SWIGLU ? kModeSwiglu : kModeGelu;
+    const bool pair = (gk == kGemmPair);
     MOE_CUDA(pair ? launch_ffn_tc2(up_mode, maps, up, st)
                   : launch_ffn_tc(up_mode, maps, up, di.num_sms, st),
              "up-projection launch");
     if (ev) MOE_CUDA(cudaEventRecord(ev[1], st), "event record");
-    // down-projection maps
     MOE_TRY(encode_rows(&maps[0], H, (uint64_t)A, c.F, "hidden rows"));
     MOE_TRY(encode_rows(&maps[1], w.W2, (uint64_t)c.E * c.d, c.F, "W2"));
     maps[2] = maps[1];
@@ -341,13 +392,6 @@ int run_expert_ffn(const moe_cfg& c, const DevInfo& di, const void* x, const int
     } else {
         maps[3] = maps[0]; maps[4] = maps[1]; maps[5] = maps[2];
     }
-    TcFfnArgs dn{};
-    dn.offsets = offsets; dn.E = c.E; dn.rows_sh = rows_sh;
-    dn.N = c.d; dn.K = c.F; dn.N_sh = c.d; dn.K_sh = c.F_shared;
-    dn.out = Ys; dn.out_sh = Sh;
-    dn.bias = c.has_bias ? (const __nv_bfloat16*)w.b2 : nullptr;
-    dn.perm_src = perm_src; dn.gate_w = topk_w;
-    dn.status = status;
     MOE_CUDA(pair ? launch_ffn_tc2(kModeDown, maps, dn, st)
                   : launch_ffn_tc(kModeDown, maps, dn, di.num_sms, st),
              "down-projection launch");

@@ -96,5 +96,10 @@ cudaError_t launch_ffn_tc(int mode, const CUtensorMap* maps, const TcFfnArgs& p,
 // ffn_tc2.cu: the same on CTA pairs (cta_group::2), 256-row tiles; same maps
 int ffn_tc2_tile_rows();
 cudaError_t launch_ffn_tc2(int mode, const CUtensorMap* maps, const TcFfnArgs& p, cudaStream_t st);
+// ffn_swap.cu: weights as the MMA's M, tokens as N, on CTA pairs.
+// maps: W, W3 (SwiGLU up; else unused), X (token rows), and the shared
+// expert's W_sh, W3_sh, X_sh; weight maps with ffn_swap_weight_box_rows rows
+int ffn_swap_weight_box_rows(int mode);
+cudaError_t launch_ffn_swap(int mode, const CUtensorMap* maps, const TcFfnArgs& p, cudaStream_t st);
 
 }  // namespace moe

@@ -18,25 +18,27 @@ WANT = ("logits", "topk_idx", "topk_w", "counts_pre", "counts_kept", "drop_mask"
 
 def _params():
     """Each small workload with the library's own GEMM choice, and the bf16
-    ones again with the 2-SM (CTA-pair) kernels forced."""
+    ones again with each tensor-core GEMM kernel forced (1-SM tokens-on-M,
+    2-SM tokens-on-M, 2-SM weights-on-M)."""
     out = list(SMALL)
-    out += [n + "@pair" for n in SMALL if small_cfg(n)["dtype"] == "bf16"]
+    for kern in ("tc1", "pair", "swap"):
+        out += [n + "@" + kern for n in SMALL if small_cfg(n)["dtype"] == "bf16"]
     return out
 
 
 @pytest.fixture(scope="module", params=_params())
 def run(request):
-    name, _, mode = request.param.partition("@")
-    old = os.environ.get("MOE_GEMM_PAIR")
-    if mode == "pair":
-        os.environ["MOE_GEMM_PAIR"] = "1"
+    name, _, kern = request.param.partition("@")
+    old = os.environ.get("MOE_GEMM_KERNEL")
+    if kern:
+        os.environ["MOE_GEMM_KERNEL"] = kern
     try:
         yield _run(name)
     finally:
         if old is None:
-            os.environ.pop("MOE_GEMM_PAIR", None)
+            os.environ.pop("MOE_GEMM_KERNEL", None)
         else:
-            os.environ["MOE_GEMM_PAIR"] = old
+            os.environ["MOE_GEMM_KERNEL"] = old
 
 
 def _run(name):
