@@ -52,6 +52,10 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--sweep", default=None,
+                    help="comma-separated token counts: time the layer at each T on the "
+                         "workload's weights for every GEMM kernel (prefill/decode crossover) "
+                         "and print one JSON line with the table instead of the bench line")
     return ap.parse_args()
 
 
@@ -84,6 +88,40 @@ def max_over_ranks(v, world):
     t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+TRAFFIC_SOURCES = ("ffn_swap.cu", "ffn_tc.cu", "ffn_tc2.cu", "ffn_tc_common.cuh", "tc_ptx.cuh",
+                   "common.cuh", "kernels.cuh")
+
+
+def kernel_sources_digest():
+    """sha256 over the GEMM kernel sources: a recorded DRAM-traffic figure is
+    reported only while the sources it was measured on are unchanged."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sparse_mixture_experts_59_b300", "csrc")
+    for name in TRAFFIC_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload, kernel):
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum)
+    recorded under profiles/ for (workload, kernel), if the kernel sources
+    still match the digest recorded with it; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic_%s.txt" % workload)
+    if not os.path.exists(path):
+        return None, None
+    digest = kernel_sources_digest()
+    with open(path) as fh:
+        for line in fh:
+            parts = line.split()
+            if len(parts) >= 4 and parts[0] == "traffic" and parts[1] == kernel:
+                if parts[3] == digest:
+                    return int(parts[2]), digest
+                return None, digest
+    return None, digest
 
 
 def measured_peaks():
@@ -234,9 +272,15 @@ def run_ours(args, world, rank, local):
     dn_s = stages["down_gemm"] / 1e3
     peak_tf = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
     up_tf = alg["up"] / up_s / 1e12
+    kname = "up_gemm/%s" % (args.gemm or "auto")
+    traffic, digest = recorded_traffic(args.workload, kname) if args.tokens is None and \
+        args.experts is None else (None, None)
     roof = {"kernel": "up-projection grouped GEMM (SwiGLU epilogue)", "bound": "tensor",
             "achieved": round(up_tf, 1), "peak": peak_tf, "unit": "TFLOP/s",
-            "frac": round(up_tf / peak_tf, 4), "traffic": None,
+            "frac": round(up_tf / peak_tf, 4), "traffic": traffic,
+            "traffic_note": "ncu dram__bytes_read.sum + dram__bytes_write.sum per launch, "
+                            "profiles/traffic_%s.txt; null if the kernel sources changed "
+                            "since (sources digest %s)" % (args.workload, digest),
             "peak_source": "%s bf16_tflops_sustained" % peak_src,
             "algorithmic_flop_per_launch": alg["up"], "launch_ms": round(stages["up_gemm"], 4),
             "frac_of_burst_peak": round(up_tf / peaks.get("bf16_tflops", 1816.0), 4)}
@@ -411,8 +455,55 @@ def run_reference(args, world, rank, local):
             "gpu_launches": 0}
 
 
+def run_sweep(args, world, local):
+    """Prefill/decode crossover: the same layer and weights at several T, each
+    GEMM kernel forced in turn, plus the library's automatic choice."""
+    dev = torch.device("cuda", local)
+    peaks, _ = measured_peaks()
+    base = workload_config(args)
+    weights = workloads.make_weights(base, dev)
+    per_expert = (3 if base["act"] == "swiglu" else 2) * base["d"] * base["F"] * 2
+    rows = []
+    for T in [int(v) for v in args.sweep.split(",")]:
+        cfg = dict(base, T=T)
+        inp = dict(weights)
+        inp["x"] = workloads.make_x(cfg, dev)
+        inp["cfg"] = cfg
+        entry = {"T": T}
+        for g in ("auto", "tc1", "swap", "pair"):
+            if g == "auto":
+                os.environ.pop("MOE_GEMM_KERNEL", None)
+            else:
+                os.environ["MOE_GEMM_KERNEL"] = g
+            layer = binding.MoeLayer(cfg, inp, device=dev)
+            outputs = {"y": torch.empty_like(inp["x"]),
+                       "counts_kept": torch.empty(cfg["E"], dtype=torch.int32, device=dev)}
+            steps = max(10, min(args.steps, 50))
+            ms, stages, _ = time_layer(layer, inp["x"], steps, args.warmup, world, outputs)
+            R = int(outputs["counts_kept"].sum().item())
+            hit = int((outputs["counts_kept"] > 0).sum().item())
+            alg = algorithmic(cfg, R)
+            gemm_ms = stages["up_gemm"] + stages["down_gemm"]
+            entry[g] = {"ms": round(ms, 4), "tokens_per_s": round(T / (ms / 1e3), 1),
+                        "gemm_ms": round(gemm_ms, 4),
+                        "gemm_tflops": round((alg["up"] + alg["down"]) / (gemm_ms / 1e3) / 1e12, 1),
+                        "weight_gbs": round(hit * per_expert / (gemm_ms / 1e3) / 1e9, 1)}
+            del layer
+        os.environ.pop("MOE_GEMM_KERNEL", None)
+        rows.append(entry)
+    return {"sweep": args.workload, "d_model": base["d"], "d_ff": base["F"], "experts": base["E"],
+            "top_k": base["k"], "hbm_peak_gbs": peaks.get("hbm_gbs"),
+            "bf16_peak_tflops_sustained": peaks.get("bf16_tflops_sustained"), "rows": rows}
+
+
 def main():
     args = parse_args()
+    if args.sweep:
+        world, rank, local = dist_init()
+        res = run_sweep(args, world, local)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        return
     if args.gemm:
         os.environ["MOE_GEMM_KERNEL"] = args.gemm
     world, rank, local = dist_init()
