@@ -90,8 +90,7 @@ def max_over_ranks(v, world):
     return float(t.item())
 
 
-TRAFFIC_SOURCES = ("ffn_swap.cu", "ffn_tc.cu", "ffn_tc2.cu", "ffn_tc_common.cuh", "tc_ptx.cuh",
-                   "common.cuh", "kernels.cuh")
+TRAFFIC_SOURCES = ("ffn_swap.cu", "ffn_tc.cu", "ffn_tc2.cu", "ffn_tc_common.cuh", "tc_ptx.cuh")
 
 
 def kernel_sources_digest():

@@ -220,7 +220,7 @@ int moe_layer_forward_profiled(const moe_cfg *cfg, const void *x, const void *Wr
  * host framework that owns every allocation and passes an operator only its
  * inputs and outputs.  This variant takes the same inputs and outputs as
  * moe_dispatch (no workspace) and keeps its scratch in a fixed device array
- * inside the library (294,912 bytes per GPU that loads the library, held
+ * inside the library (393,472 bytes per GPU that loads the library, held
  * until the process exits); it allocates nothing.
  *  - T*k must be <= 65536; larger calls return MOE_ERR_INVALID_ARG and launch
  *    nothing.
@@ -241,6 +241,15 @@ int moe_dispatch_noalloc(const moe_cfg *cfg, const int *topk_idx, const float *p
 /* Reads (and leaves) the device status word of a workspace: MOE_OK, or the
  * first MOE_ERR_DEVICE_* recorded since the last init.  Synchronises `stream`. */
 int moe_get_device_status(void *ws, size_t ws_bytes, void *stream, int *status);
+
+/* Test hook for the failure path of dispatch's bounded waits (no
+ * counterpart on the pages).  The next moe_dispatch / moe_layer_forward on
+ * this workspace runs with look-back block `block` (each block covers 512
+ * consecutive assignments) never publishing its counts, so the blocks after
+ * it wait about a second, give up, and record MOE_ERR_DEVICE_TIMEOUT in the
+ * device status; their outputs are then not meaningful.  The hook clears
+ * itself; re-initialise the workspace before further use. */
+int moe_test_hold_lookback_block(void *ws, size_t ws_bytes, int block, void *stream);
 
 #ifdef __cplusplus
 }

@@ -21,7 +21,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 EXPORTS = ("moe_status_string", "moe_last_error", "moe_capacity", "moe_workspace_size",
            "moe_workspace_init", "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine",
            "moe_layer_forward", "moe_layer_forward_profiled", "moe_get_device_status",
-           "moe_dispatch_noalloc")
+           "moe_dispatch_noalloc", "moe_test_hold_lookback_block")
 
 
 class MoeError(RuntimeError):
@@ -75,6 +75,7 @@ def lib():
         L.moe_layer_forward_profiled.argtypes = [P, P, P, P, P, P, P, S, P, P]
         L.moe_get_device_status.argtypes = [P, S, P, ctypes.POINTER(I)]
         L.moe_dispatch_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P]
+        L.moe_test_hold_lookback_block.argtypes = [P, S, I, P]
         for name in EXPORTS:
             getattr(L, name).restype = getattr(L, name).restype or I
         _lib = L
@@ -253,6 +254,12 @@ def layer_forward(cfg, x, Wr, weights: dict, logit_bias=None, ws=None, outputs=N
                                                 ctypes.byref(w), ctypes.byref(out_s), _p(ws),
                                                 ws.numel(), _stream(stream), ev))
     return o
+
+
+def test_hold_lookback_block(ws, block, stream=None):
+    """Test hook: the next dispatch on `ws` runs with look-back block `block`
+    never publishing, so later blocks time out (MOE_ERR_DEVICE_TIMEOUT)."""
+    _check(lib().moe_test_hold_lookback_block(_p(ws), ws.numel(), int(block), _stream(stream)))
 
 
 def device_status(ws, stream=None) -> int:

@@ -32,7 +32,7 @@ size_t esize(const moe_cfg& c) { return c.dtype == MOE_F32 ? 4 : 2; }
 size_t align_up(size_t v) { return (v + 255) & ~(size_t)255; }
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-constexpr int kRouterTopkMaxBlocks = 1024;
+constexpr int kRouterTopkMaxBlocks = 148;   // P partial sums to add up at the end
 int router_blocks(int T) {
     const int b = (T + 7) / 8;
     return b < 1 ? 1 : (b > kRouterTopkMaxBlocks ? kRouterTopkMaxBlocks : b);
@@ -590,6 +590,18 @@ int moe_layer_forward_profiled(const moe_cfg* cfg, const void* x, const void* Wr
     for (int i = 0; i < 7; ++i)
         if (!events[i]) return fail(MOE_ERR_INVALID_ARG, "events[i] is NULL%s");
     return layer_forward_impl(cfg, x, Wr, logit_bias, w, out, ws, ws_bytes, stream, events);
+}
+
+int moe_test_hold_lookback_block(void* ws, size_t ws_bytes, int block, void* stream) {
+    if (!ws) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL%s");
+    if (ws_bytes < kCtrlWords * 4) return fail(MOE_ERR_WORKSPACE, "workspace too small%s");
+    if (block < 0) return fail(MOE_ERR_INVALID_ARG, "block must be >= 0%s");
+    static thread_local int value;      // pageable source; the copy is staged at enqueue
+    value = block + 1;
+    MOE_CUDA(cudaMemcpyAsync(at<int>(ws, 0) + kCtrlHoldBlock, &value, sizeof(int),
+                             cudaMemcpyHostToDevice, (cudaStream_t)stream),
+             "hold-block write");
+    return MOE_OK;
 }
 
 int moe_get_device_status(void* ws, size_t ws_bytes, void* stream, int* status) {

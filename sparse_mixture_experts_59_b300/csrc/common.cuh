@@ -19,6 +19,7 @@ enum CtrlWord {
     kCtrlDispatchTicket = 1,
     kCtrlDispatchDone = 2,
     kCtrlRouterDone = 3,
+    kCtrlHoldBlock = 4,     // test hook: look-back block (id + 1) that never publishes
     kCtrlWords = 64
 };
 

@@ -94,15 +94,18 @@ dispatch_rank_kernel(const int* __restrict__ topk_idx, int A, int Ttok, int E,
         my_rank[it] = (e >= 0) ? s_cnt[buf][warp][e] + in_warp : -1;
     }
 
-    // decoupled look-back, one thread per expert
+    // decoupled look-back, one thread per expert.  A block named by the
+    // kCtrlHoldBlock test hook publishes nothing, so its successors' bounded
+    // waits run out and report MOE_ERR_DEVICE_TIMEOUT.
+    const bool hold = ctrl[kCtrlHoldBlock] == bid + 1;
     if (tid < E) {
         const unsigned agg = (unsigned)s_run[tid];
         unsigned* mine = tile_status + (size_t)bid * E + tid;
         if (bid == 0) {
             s_excl[tid] = 0;
-            st_release_u32(mine, kFlagPrefix | agg);
+            if (!hold) st_release_u32(mine, kFlagPrefix | agg);
         } else {
-            st_release_u32(mine, kFlagAgg | agg);
+            if (!hold) st_release_u32(mine, kFlagAgg | agg);
             unsigned excl = 0;
             int j = bid - 1;
             long long t0 = 0;
@@ -122,7 +125,7 @@ dispatch_rank_kernel(const int* __restrict__ topk_idx, int A, int Ttok, int E,
             }
             if (timed_out) raise_error(status, MOE_ERR_DEVICE_TIMEOUT);
             s_excl[tid] = (int)excl;
-            st_release_u32(mine, kFlagPrefix | ((excl + agg) & kValueMask));
+            if (!hold) st_release_u32(mine, kFlagPrefix | ((excl + agg) & kValueMask));
         }
     }
     __syncthreads();
@@ -177,6 +180,7 @@ dispatch_rank_kernel(const int* __restrict__ topk_idx, int A, int Ttok, int E,
         }
         ctrl[kCtrlDispatchTicket] = 0;
         ctrl[kCtrlDispatchDone] = 0;
+        ctrl[kCtrlHoldBlock] = 0;
     }
     // clear the look-back state for the next call
     for (int i = tid; i < nblk * E; i += kDspThreads) tile_status[i] = 0u;

@@ -23,8 +23,9 @@ constexpr size_t kMaxBlocks =
     (size_t)(kNoAllocMaxAssignments + moe::kDspChunk - 1) / moe::kDspChunk;
 constexpr size_t kStatusBytes = kMaxBlocks * moe::kMaxExperts * 4;
 constexpr size_t kRankBytes = (size_t)kNoAllocMaxAssignments * 4;
-constexpr size_t kScratchBytes = kCtrlBytes + kStatusBytes + kRankBytes;   // 294,912 bytes
+constexpr size_t kScratchBytes = kCtrlBytes + kStatusBytes + kRankBytes;   // 393,472 bytes
 static_assert(kCtrlBytes % 256 == 0 && kStatusBytes % 256 == 0, "scratch regions stay aligned");
+static_assert(kScratchBytes == 393472, "the size stated in include/moe.h");
 
 // Shared by every call on a device; keeps the last call's contents.
 static __device__ __align__(256) unsigned char g_dispatch_scratch[kScratchBytes];

@@ -12,7 +12,7 @@ namespace moe {
 enum FfnMode { kModeSwiglu = 0, kModeGelu = 1, kModeDown = 2 };
 
 // dispatch geometry: assignments per block
-constexpr int kDspItems = 8;
+constexpr int kDspItems = 2;
 constexpr int kDspChunk = 256 * kDspItems;
 inline int dispatch_blocks(int A) { return A > 0 ? (A + kDspChunk - 1) / kDspChunk : 1; }
 

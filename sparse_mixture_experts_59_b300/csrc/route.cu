@@ -174,10 +174,22 @@ router_topk_kernel(const float* part, int nsplit, const float* __restrict__ bias
     __syncthreads();
     if (!s_last) return;
     __threadfence();
+    // column sums of prob_part[nblocks][E]: thread t adds rows g, g+G, ...
+    // (g = t / E, G = 256 / E groups) for expert t % E, then the groups are
+    // added in order -- a fixed order, so the result repeats exactly
+    const int G = blockDim.x / E > 0 ? (int)blockDim.x / E : 1;
+    float* s_col = &s_psum[0][0];                  // reuse: [G][E] partial columns
+    if ((int)threadIdx.x < G * E) {
+        const int e = threadIdx.x % E, g = threadIdx.x / E;
+        float acc = 0.f;
+        for (int b = g; b < (int)gridDim.x; b += G) acc += __ldcg(prob_part + (size_t)b * E + e);
+        s_col[g * E + e] = acc;
+    }
+    __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        float s = 0.f;
-        for (int b = 0; b < (int)gridDim.x; ++b) s += __ldcg(prob_part + (size_t)b * E + e);
-        prob_mean[e] = s / (float)Ttok;
+        float acc = 0.f;
+        for (int g = 0; g < G; ++g) acc += s_col[g * E + e];
+        prob_mean[e] = acc / (float)Ttok;
     }
     if (threadIdx.x == 0) *done_counter = 0;   // leave the workspace reusable
 }

@@ -116,3 +116,27 @@ def test_out_of_range_expert_index_is_reported():
     ref = oracle.dispatch(idx.numpy(), 8, -1)
     np.testing.assert_array_equal(do["dest"].cpu().numpy(), ref["dest"])
     assert binding.device_status(ws) == 0
+
+
+def test_lookback_wait_times_out_and_reports():
+    """Failure path of dispatch's bounded waits: with one look-back block held
+    back (its flag is never set), the blocks after it give up after about a
+    second, the device status reads MOE_ERR_DEVICE_TIMEOUT, and the context
+    stays usable for the next call."""
+    import time
+    cfg = workloads.config("mixtral_prefill", T=2048, d=64, F=64, E=8, k=2)   # 8 blocks
+    c = binding.make_config(cfg)
+    g = torch.Generator().manual_seed(9)
+    idx = torch.stack([torch.randperm(8, generator=g)[:2] for _ in range(2048)]).to(torch.int32)
+    ws = binding.new_workspace(c)
+    binding.test_hold_lookback_block(ws, 2)
+    t0 = time.time()
+    binding.dispatch(c, idx.cuda(), ws=ws)
+    status = binding.device_status(ws)
+    assert status == 5                                 # MOE_ERR_DEVICE_TIMEOUT
+    assert time.time() - t0 < 60
+    ws = binding.new_workspace(c)
+    do = binding.dispatch(c, idx.cuda(), ws=ws)
+    ref = oracle.dispatch(idx.numpy(), 8, -1)
+    np.testing.assert_array_equal(do["dest"].cpu().numpy(), ref["dest"])
+    assert binding.device_status(ws) == 0
