@@ -46,6 +46,8 @@ def parse_args():
     ap.add_argument("--decode-workload", default="mixtral_decode")
     ap.add_argument("--tokens", type=int, default=None, help="override T (profiling cases)")
     ap.add_argument("--experts", type=int, default=None, help="override E (profiling cases)")
+    ap.add_argument("--no-pdl", action="store_true",
+                    help="launch without programmatic dependent launch (MOE_PDL=0)")
     ap.add_argument("--gemm", default=None, choices=["tc1", "pair", "swap"],
                     help="force the expert GEMM kernel (default: the library's choice)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -209,16 +211,16 @@ def algorithmic(cfg, R):
 
 
 def time_layer(layer, x, steps, warmup, world, outputs, clocks=None):
+    """Times `steps` plain layer calls (the step time), then the same number of
+    calls that record CUDA events at every stage boundary on the launching
+    stream (the per-kernel times: events between kernels can keep a kernel
+    from starting early, so they stay out of the step time)."""
     for _ in range(warmup):
         layer.forward(x, outputs=outputs)
     torch.cuda.synchronize()
     st = binding.device_status(layer.ws)
     if st != 0:
         raise RuntimeError("device status %d after warm-up" % st)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(steps)]
-    for row in evs:
-        for e in row:
-            e.record()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     barrier(world)
@@ -226,20 +228,35 @@ def time_layer(layer, x, steps, warmup, world, outputs, clocks=None):
     if clocks:
         clocks.start()
     start.record()
+    for _ in range(steps):
+        layer.forward(x, outputs=outputs)
+    end.record()
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / steps
+    # profiled pass: stage boundaries
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(steps)]
+    for row in evs:
+        for e in row:
+            e.record()
+    pstart, pend = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    pstart.record()
     for i in range(steps):
         layer.forward(x, outputs=outputs, events=evs[i])
-    end.record()
+    pend.record()
     torch.cuda.synchronize()
     clk = clocks.stop() if clocks else None
     barrier(world)
     torch.cuda.synchronize()
-    ms = start.elapsed_time(end) / steps
+    ms_prof = pstart.elapsed_time(pend) / steps
     stages = np.array([[row[j].elapsed_time(row[j + 1]) for j in range(6)] for row in evs])
     names = ("router", "dispatch", "gather", "up_gemm", "down_gemm", "combine")
     st = binding.device_status(layer.ws)
     if st != 0:
         raise RuntimeError("device status %d after timed steps" % st)
-    return ms, {n: float(stages[:, j].mean()) for j, n in enumerate(names)}, clk
+    out = {n: float(stages[:, j].mean()) for j, n in enumerate(names)}
+    out["step_profiled"] = float(ms_prof)
+    return ms, out, clk
 
 
 def workload_config(args):
@@ -302,8 +319,11 @@ def run_ours(args, world, rank, local):
                          "peak": peak_tf, "up_ms": round(stages["up_gemm"], 4),
                          "down_ms": round(stages["down_gemm"], 4)},
         "stage_ms": {k: round(v, 4) for k, v in stages.items()},
+        "timing": "value from %d plain layer calls; stage_ms and the roofline's launch_ms from "
+                  "%d more calls with CUDA events at the stage boundaries" % (args.steps, args.steps),
         "layer_tflops": round(alg["total"] / (ms / 1e3) / 1e12, 1),
         "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "pdl": os.environ.get("MOE_PDL", "1") != "0",
         "clocks": clk,
     }
 
@@ -505,6 +525,8 @@ def main():
         return
     if args.gemm:
         os.environ["MOE_GEMM_KERNEL"] = args.gemm
+    if args.no_pdl:
+        os.environ["MOE_PDL"] = "0"
     world, rank, local = dist_init()
     if args.impl == "reference":
         if rank == 0:

@@ -27,6 +27,17 @@ enum CtrlWord {
 // these kernels last microseconds.
 constexpr long long kWaitLimitCycles = 2000000000LL;
 
+// Programmatic dependent launch.  Every kernel of the layer is launched so
+// that it may start while its stream predecessor finishes: it does its
+// on-chip set-up, then pdl_wait() before its first global-memory access (that
+// returns once the predecessor grid has completed and its writes are
+// visible), then pdl_trigger() so that its own successor may be scheduled.
+// Without the launch attribute both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void raise_error(int* status, int code) {
     if (status) atomicCAS(status, 0, code);
 }

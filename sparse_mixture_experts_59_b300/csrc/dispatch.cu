@@ -19,6 +19,7 @@
 // Kernel 2 (dispatch_scatter_kernel): dest / perm_src / drop mask.
 #include "common.cuh"
 #include "kernels.cuh"
+#include "launch.cuh"
 
 namespace moe {
 
@@ -51,6 +52,8 @@ dispatch_rank_kernel(const int* __restrict__ topk_idx, int A, int Ttok, int E,
     int* status = ctrl + kCtrlStatus;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_wait();
+    pdl_trigger();
     if (tid == 0) s_bid = atomicAdd(ctrl + kCtrlDispatchTicket, 1);
     if (tid < E) s_run[tid] = 0;
     __syncthreads();
@@ -191,6 +194,8 @@ dispatch_scatter_kernel(const int* __restrict__ topk_idx, const int* __restrict_
                         int E, long long cap, const int* __restrict__ offsets,
                         int* __restrict__ dest, int* __restrict__ perm_src,
                         unsigned char* __restrict__ drop_mask, int* __restrict__ status) {
+    pdl_wait();
+    pdl_trigger();
     for (int a = blockIdx.x * blockDim.x + threadIdx.x; a < A; a += gridDim.x * blockDim.x) {
         const int e = topk_idx[a];
         const int r = rank[a];
@@ -218,17 +223,16 @@ cudaError_t launch_dispatch(const int* topk_idx, int T, int k, int E, long long 
                             int num_sms, cudaStream_t st) {
     const int A = T * k;
     const int nblk = dispatch_blocks(A);
-    dispatch_rank_kernel<<<nblk, kDspThreads, 0, st>>>(topk_idx, A, T, E, cap, tile_status, ctrl,
-                                                       rank, counts_pre, counts_kept, offsets,
-                                                       prob_mean, stats);
-    cudaError_t err = cudaGetLastError();
+    cudaError_t err = launch_kernel(dispatch_rank_kernel, dim3(nblk), dim3(kDspThreads), 0, st, 1,
+                                    topk_idx, A, T, E, cap, tile_status, ctrl, rank, counts_pre,
+                                    counts_kept, offsets, prob_mean, stats);
     if (err != cudaSuccess) return err;
     int sblk = (A + 255) / 256;
     if (sblk > num_sms * 8) sblk = num_sms * 8;
     if (sblk < 1) sblk = 1;
-    dispatch_scatter_kernel<<<sblk, 256, 0, st>>>(topk_idx, rank, A, E, cap, offsets, dest,
-                                                  perm_src, drop_mask, ctrl + kCtrlStatus);
-    return cudaGetLastError();
+    return launch_kernel(dispatch_scatter_kernel, dim3(sblk), dim3(256), 0, st, 1, topk_idx,
+                         (const int*)rank, A, E, cap, (const int*)offsets, dest, perm_src, drop_mask,
+                         ctrl + kCtrlStatus);
 }
 
 }  // namespace moe

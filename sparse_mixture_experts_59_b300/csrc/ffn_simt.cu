@@ -11,6 +11,7 @@
 //   down: Ys[perm_src[r]] = topk_w[perm_src[r]] * (H[r] W2^T + b2);  shared: Sh = H_sh S2^T
 #include "common.cuh"
 #include "kernels.cuh"
+#include "launch.cuh"
 
 namespace moe {
 
@@ -25,6 +26,8 @@ __global__ void __launch_bounds__(256) ffn_simt_kernel(SimtFfnArgs p) {
 
     const int nt_r = (p.N + kSimtBN - 1) / kSimtBN;
     const int nt_s = p.rows_sh > 0 ? (p.N_sh + kSimtBN - 1) / kSimtBN : 0;
+    pdl_wait();
+    pdl_trigger();
     group_tile_prefix(p.offsets, p.E, p.rows_sh, kSimtBM, nt_r, nt_s, s_start);
     const int G = p.E + (p.rows_sh > 0 ? 1 : 0);
     const int tile = blockIdx.x;
@@ -125,10 +128,9 @@ cudaError_t launch_ffn_simt(int mode, const SimtFfnArgs& p, int A_rows, cudaStre
                              (long long)((p.rows_sh + kSimtBM - 1) / kSimtBM) * nt_s;
     if (blocks <= 0) return cudaSuccess;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    if (mode == kModeSwiglu) ffn_simt_kernel<kModeSwiglu><<<(int)blocks, 256, 0, st>>>(p);
-    else if (mode == kModeGelu) ffn_simt_kernel<kModeGelu><<<(int)blocks, 256, 0, st>>>(p);
-    else ffn_simt_kernel<kModeDown><<<(int)blocks, 256, 0, st>>>(p);
-    return cudaGetLastError();
+    auto kernel = mode == kModeSwiglu ? ffn_simt_kernel<kModeSwiglu>
+                : mode == kModeGelu ? ffn_simt_kernel<kModeGelu> : ffn_simt_kernel<kModeDown>;
+    return launch_kernel(kernel, dim3((unsigned)blocks), dim3(256), 0, st, 1, p);
 }
 
 }  // namespace moe

@@ -22,6 +22,7 @@
 // rows with 16-byte stores (down: to the assignment's slot, gate-scaled).
 #include "common.cuh"
 #include "kernels.cuh"
+#include "launch.cuh"
 #include "tc_ptx.cuh"
 
 namespace moe {
@@ -150,6 +151,8 @@ ffn_swap_kernel(const __grid_constant__ CUtensorMap mapW, const __grid_constant_
         ptx::tmem_alloc_pair(s_tmem, TMEM_COLS);
         ptx::tmem_relinquish_pair();
     }
+    pdl_wait();       // offsets and the token rows come from the preceding kernels
+    pdl_trigger();
     for (int i = threadIdx.x; i <= p.E; i += NUM_THREADS) s_off[i] = p.offsets[i];
     constexpr int UNITS = SwapTraits<MODE>::UNITS;
     const int nw_r = (p.N + UNITS - 1) / UNITS;
@@ -371,10 +374,8 @@ cudaError_t launch_mode(const CUtensorMap* maps, const TcFfnArgs& p, cudaStream_
         if (clusters < 1) return cudaErrorInvalidConfiguration;
         if (dev >= 0 && dev < 64) cached[dev] = clusters;
     }
-    cfg.gridDim = dim3(2 * clusters);
-    err = cudaLaunchKernelEx(&cfg, kernel, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
-    if (err != cudaSuccess) return err;
-    return cudaGetLastError();
+    return launch_kernel(kernel, dim3(2 * clusters), dim3(NUM_THREADS), SMEM_BYTES, st, 2, maps[0],
+                         maps[1], maps[2], maps[3], maps[4], maps[5], p);
 }
 
 }  // namespace

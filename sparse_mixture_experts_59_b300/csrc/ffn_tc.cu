@@ -30,6 +30,7 @@
 // tile reads (the next segment, or TMA's zero fill) and never stored.
 #include "common.cuh"
 #include "kernels.cuh"
+#include "launch.cuh"
 #include "ffn_tc_common.cuh"
 #include "tc_ptx.cuh"
 
@@ -106,6 +107,8 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
         ptx::tmem_alloc(s_tmem, TMEM_COLS);
         ptx::tmem_relinquish();
     }
+    pdl_wait();       // offsets and the A rows come from the preceding kernels
+    pdl_trigger();
     for (int i = threadIdx.x; i <= p.E; i += NUM_THREADS) s_off[i] = p.offsets[i];
     const int nt_r = (p.N + BN_OUT - 1) / BN_OUT;
     const int nt_s = p.rows_sh > 0 ? (p.N_sh + BN_OUT - 1) / BN_OUT : 0;
@@ -224,19 +227,13 @@ int ffn_tc_smem_bytes() { return SMEM_BYTES; }
 
 cudaError_t launch_ffn_tc(int mode, const CUtensorMap* maps, const TcFfnArgs& p, int num_sms,
                           cudaStream_t st) {
-    cudaError_t err;
-    const dim3 grid(num_sms), block(NUM_THREADS);
-#define MOE_TC_LAUNCH(M)                                                                        \
-    err = cudaFuncSetAttribute(ffn_tc_kernel<M>, cudaFuncAttributeMaxDynamicSharedMemorySize,   \
-                               SMEM_BYTES);                                                     \
-    if (err != cudaSuccess) return err;                                                         \
-    ffn_tc_kernel<M><<<grid, block, SMEM_BYTES, st>>>(maps[0], maps[1], maps[2], maps[3],       \
-                                                      maps[4], maps[5], p);
-    if (mode == kModeSwiglu) { MOE_TC_LAUNCH(kModeSwiglu) }
-    else if (mode == kModeGelu) { MOE_TC_LAUNCH(kModeGelu) }
-    else { MOE_TC_LAUNCH(kModeDown) }
-#undef MOE_TC_LAUNCH
-    return cudaGetLastError();
+    auto kernel = mode == kModeSwiglu ? ffn_tc_kernel<kModeSwiglu>
+                : mode == kModeGelu ? ffn_tc_kernel<kModeGelu> : ffn_tc_kernel<kModeDown>;
+    const cudaError_t err =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (err != cudaSuccess) return err;
+    return launch_kernel(kernel, dim3(num_sms), dim3(NUM_THREADS), SMEM_BYTES, st, 1, maps[0],
+                         maps[1], maps[2], maps[3], maps[4], maps[5], p);
 }
 
 }  // namespace moe

@@ -19,6 +19,7 @@
 #include "common.cuh"
 #include "ffn_tc_common.cuh"
 #include "kernels.cuh"
+#include "launch.cuh"
 #include "tc_ptx.cuh"
 
 namespace moe {
@@ -100,6 +101,8 @@ ffn_tc2_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
         ptx::tmem_alloc_pair(s_tmem, TMEM_COLS);
         ptx::tmem_relinquish_pair();
     }
+    pdl_wait();       // offsets and the token rows come from the preceding kernels
+    pdl_trigger();
     for (int i = threadIdx.x; i <= p.E; i += NUM_THREADS) s_off[i] = p.offsets[i];
     const int nt_r = (p.N + BN_OUT - 1) / BN_OUT;
     const int nt_s = p.rows_sh > 0 ? (p.N_sh + BN_OUT - 1) / BN_OUT : 0;
@@ -252,10 +255,8 @@ cudaError_t launch_mode(const CUtensorMap* maps, const TcFfnArgs& p, cudaStream_
         if (clusters < 1) return cudaErrorInvalidConfiguration;
         if (dev >= 0 && dev < 64) cached[dev] = clusters;
     }
-    cfg.gridDim = dim3(2 * clusters);
-    err = cudaLaunchKernelEx(&cfg, kernel, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
-    if (err != cudaSuccess) return err;
-    return cudaGetLastError();
+    return launch_kernel(kernel, dim3(2 * clusters), dim3(NUM_THREADS), SMEM_BYTES, st, 2, maps[0],
+                         maps[1], maps[2], maps[3], maps[4], maps[5], p);
 }
 
 }  // namespace

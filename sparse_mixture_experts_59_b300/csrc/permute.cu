@@ -9,6 +9,7 @@
 // bandwidth-bound and carry no arithmetic beyond the fp32 sum of the combine.
 #include "common.cuh"
 #include "kernels.cuh"
+#include "launch.cuh"
 
 namespace moe {
 
@@ -18,6 +19,8 @@ __global__ void __launch_bounds__(256)
 gather_rows_kernel(const uint4* __restrict__ x, const int* __restrict__ perm_src,
                    const int* __restrict__ offsets, int E, int k, int Ttok, int vec_per_row,
                    uint4* __restrict__ Xp, int* __restrict__ status) {
+    pdl_wait();
+    pdl_trigger();
     const int R = offsets[E];
     const int warps = (gridDim.x * blockDim.x) >> 5;
     const int lane = threadIdx.x & 31;
@@ -43,6 +46,8 @@ combine_kernel(const T* __restrict__ x, const T* __restrict__ Ys,
                T* __restrict__ y, int Ttok, int d, int k) {
     constexpr int NV = Vec16<T>::N;
     const int vec_per_row = d / NV;
+    pdl_wait();
+    pdl_trigger();
     const long long total = (long long)Ttok * vec_per_row;
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += (long long)gridDim.x * blockDim.x) {
@@ -82,9 +87,8 @@ cudaError_t launch_gather(int dtype, const void* x, const int* perm_src, const i
     long long blocks = ((long long)A * 32 + 255) / 256;
     if (blocks > num_sms * 16) blocks = num_sms * 16;
     if (blocks < 1) blocks = 1;
-    gather_rows_kernel<<<(int)blocks, 256, 0, st>>>((const uint4*)x, perm_src, offsets, E, k, T, vpr,
-                                                    (uint4*)Xp, status);
-    return cudaGetLastError();
+    return launch_kernel(gather_rows_kernel, dim3((unsigned)blocks), dim3(256), 0, st, 1,
+                         (const uint4*)x, perm_src, offsets, E, k, T, vpr, (uint4*)Xp, status);
 }
 
 cudaError_t launch_combine(int dtype, const void* x, const void* Ys, const unsigned char* drop_mask,
@@ -96,14 +100,12 @@ cudaError_t launch_combine(int dtype, const void* x, const void* Ys, const unsig
     if (blocks > num_sms * 16) blocks = num_sms * 16;
     if (blocks < 1) blocks = 1;
     if (dtype == MOE_F32)
-        combine_kernel<float><<<(int)blocks, 256, 0, st>>>((const float*)x, (const float*)Ys,
-                                                           drop_mask, (const float*)Sh, (float*)y,
-                                                           T, d, k);
-    else
-        combine_kernel<__nv_bfloat16><<<(int)blocks, 256, 0, st>>>(
-            (const __nv_bfloat16*)x, (const __nv_bfloat16*)Ys, drop_mask,
-            (const __nv_bfloat16*)Sh, (__nv_bfloat16*)y, T, d, k);
-    return cudaGetLastError();
+        return launch_kernel(combine_kernel<float>, dim3((unsigned)blocks), dim3(256), 0, st, 1,
+                             (const float*)x, (const float*)Ys, drop_mask, (const float*)Sh,
+                             (float*)y, T, d, k);
+    return launch_kernel(combine_kernel<__nv_bfloat16>, dim3((unsigned)blocks), dim3(256), 0, st, 1,
+                         (const __nv_bfloat16*)x, (const __nv_bfloat16*)Ys, drop_mask,
+                         (const __nv_bfloat16*)Sh, (__nv_bfloat16*)y, T, d, k);
 }
 
 }  // namespace moe

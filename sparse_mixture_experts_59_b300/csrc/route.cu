@@ -10,6 +10,7 @@
 // balancing and expert collapse".
 #include "common.cuh"
 #include "kernels.cuh"
+#include "launch.cuh"
 
 namespace moe {
 
@@ -27,6 +28,8 @@ router_logits_simt(const T* __restrict__ x, const T* __restrict__ Wr,
     __shared__ __align__(16) float Ws[BK][BN + 4];
     const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    pdl_wait();
+    pdl_trigger();
     float acc[4][4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -86,6 +89,8 @@ router_topk_kernel(const float* part, int nsplit, const float* __restrict__ bias
     const bool want_p = prob_mean != nullptr;
     if (want_p)
         for (int e = lane; e < E; e += 32) s_psum[warp][e] = 0.f;
+    pdl_wait();
+    pdl_trigger();
 
     for (int t = blockIdx.x * WARPS + warp; t < Ttok; t += gridDim.x * WARPS) {
         float l[VPL];
@@ -199,12 +204,10 @@ cudaError_t launch_router_logits_simt(int dtype, const void* x, const void* Wr, 
                                       float* logits, int T, int d, int E, cudaStream_t st) {
     dim3 grid((T + 63) / 64, (E + 63) / 64);
     if (dtype == MOE_F32)
-        router_logits_simt<float><<<grid, 256, 0, st>>>((const float*)x, (const float*)Wr, bias,
-                                                        logits, T, d, E);
-    else
-        router_logits_simt<__nv_bfloat16><<<grid, 256, 0, st>>>(
-            (const __nv_bfloat16*)x, (const __nv_bfloat16*)Wr, bias, logits, T, d, E);
-    return cudaGetLastError();
+        return launch_kernel(router_logits_simt<float>, grid, dim3(256), 0, st, 1,
+                             (const float*)x, (const float*)Wr, bias, logits, T, d, E);
+    return launch_kernel(router_logits_simt<__nv_bfloat16>, grid, dim3(256), 0, st, 1,
+                         (const __nv_bfloat16*)x, (const __nv_bfloat16*)Wr, bias, logits, T, d, E);
 }
 
 cudaError_t launch_router_topk(const float* part, int nsplit, const float* bias, float* logits,
@@ -212,30 +215,11 @@ cudaError_t launch_router_topk(const float* part, int nsplit, const float* bias,
                                float* prob_part, float* prob_mean, int* done, int nblocks,
                                cudaStream_t st) {
     const int vpl = (E + 31) / 32;
-#define MOE_TOPK_CASE(V)                                                                  \
-    case V:                                                                               \
-        router_topk_kernel<V><<<nblocks, 256, 0, st>>>(part, nsplit, bias, logits, T, E, k,   \
-                                                       topk_idx, topk_w, prob_part,       \
-                                                       prob_mean, done);                  \
-        break;
-    switch (vpl) {
-        MOE_TOPK_CASE(1)
-        MOE_TOPK_CASE(2)
-        MOE_TOPK_CASE(4)
-        MOE_TOPK_CASE(8)
-        case 3:
-            router_topk_kernel<4><<<nblocks, 256, 0, st>>>(part, nsplit, bias, logits, T, E, k,
-                                                           topk_idx, topk_w, prob_part, prob_mean,
-                                                           done);
-            break;
-        default:
-            router_topk_kernel<8><<<nblocks, 256, 0, st>>>(part, nsplit, bias, logits, T, E, k,
-                                                           topk_idx, topk_w, prob_part, prob_mean,
-                                                           done);
-            break;
-    }
-#undef MOE_TOPK_CASE
-    return cudaGetLastError();
+    auto kernel = vpl <= 1 ? router_topk_kernel<1>
+                : vpl <= 2 ? router_topk_kernel<2>
+                : vpl <= 4 ? router_topk_kernel<4> : router_topk_kernel<8>;
+    return launch_kernel(kernel, dim3(nblocks), dim3(256), 0, st, 1, part, nsplit, bias, logits, T,
+                         E, k, topk_idx, topk_w, prob_part, prob_mean, done);
 }
 
 }  // namespace moe

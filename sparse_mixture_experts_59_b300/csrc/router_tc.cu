@@ -15,6 +15,7 @@
 // same on every run.
 #include "common.cuh"
 #include "kernels.cuh"
+#include "launch.cuh"
 #include "tc_ptx.cuh"
 
 namespace moe {
@@ -70,6 +71,8 @@ router_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constan
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *s_tmem;
+    pdl_wait();       // x may come from the preceding kernel; part is reused across calls
+    pdl_trigger();
 
     if (warp == 0 && lane == 0) {
         bool ok = true;
@@ -173,9 +176,8 @@ cudaError_t launch_router_tc(const CUtensorMap& map_x, const CUtensorMap& map_w,
     cudaError_t err = cudaFuncSetAttribute(router_tc_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem);
     if (err != cudaSuccess) return err;
-    router_tc_kernel<<<dim3(p.m_tiles, p.splits), 128, p.smem, st>>>(
-        map_x, map_w, T, E, p.NB, p.nkb, p.kb_per_split, part, status);
-    return cudaGetLastError();
+    return launch_kernel(router_tc_kernel, dim3(p.m_tiles, p.splits), dim3(128), p.smem, st, 1,
+                         map_x, map_w, T, E, p.NB, p.nkb, p.kb_per_split, part, status);
 }
 
 }  // namespace moe
