@@ -70,6 +70,7 @@ enum moe_status {
 
 enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 };
 enum moe_act { MOE_GELU_ERF = 0, MOE_SWIGLU = 1 };
+enum moe_scoring { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 };
 
 /* Layer shape and options.
  *  T        tokens (>= 0; T = 0 is a no-op)
@@ -85,7 +86,13 @@ enum moe_act { MOE_GELU_ERF = 0, MOE_SWIGLU = 1 };
  *  has_bias GELU experts carry b1, b2 (SwiGLU experts take none)
  *  capacity_factor  > 0: capacity = max(1, floor(cf*T*k/E)) assignments per
  *           expert ("The Capacity Factor"); later assignments, in token order,
- *           are dropped and add nothing.  <= 0: dropless. */
+ *           are dropped and add nothing.  <= 0: dropless.
+ *  scoring  MOE_SCORE_SOFTMAX (default): softmax over all E experts;
+ *           MOE_SCORE_SIGMOID: an independent sigmoid per expert
+ *           ("Mixture-of-Experts routing", "The knobs": scoring_func)
+ *  no_renorm 0 (default): kept scores divided by their sum; 1: kept scores
+ *           used as they are (the same page's norm_topk_prob = false)
+ * A zero-filled moe_cfg with the sizes set gives the pages' default router. */
 typedef struct moe_cfg {
     int T, d, F, E, k;
     int F_shared;
@@ -93,6 +100,8 @@ typedef struct moe_cfg {
     int act;
     int has_bias;
     float capacity_factor;
+    int scoring;
+    int no_renorm;
 } moe_cfg;
 
 /* Expert weights (device pointers, dtype of the layer).  W3 only for SwiGLU;
@@ -145,9 +154,11 @@ int moe_workspace_init(const moe_cfg *cfg, void *ws, size_t ws_bytes, void *stre
 
 /* Router ("The Gating Mechanism"; "The router"):
  *   logits[t,e] = sum_i x[t,i] Wr[e,i] (+ logit_bias[e])      fp32 [T,E]
- *   p[t,:] = softmax(logits[t,:]) over all E experts
+ *   p[t,:] = softmax(logits[t,:]) over all E experts (sigmoid(logits) per
+ *            expert with MOE_SCORE_SIGMOID)
  *   topk_idx[t,:] = the k largest logits, descending, ties to the lower index
  *   topk_w[t,s] = p[t,topk_idx[t,s]] / sum_s' p[t,topk_idx[t,s']]
+ *            (p[t,topk_idx[t,s]] itself with no_renorm)
  *   prob_mean[e] = mean over t of p[t,e]   (P_e of the aux loss; may be NULL)
  * x [T,d] and Wr [E,d] in the layer dtype; logit_bias [E] fp32 or NULL (a
  * fixed per-expert offset on the logits). */

@@ -28,6 +28,7 @@ def _load():
         P, I, D, LL = ctypes.c_void_p, ctypes.c_int, ctypes.c_double, ctypes.c_longlong
         lib.oracle_router_logits.argtypes = [I, P, I, I, I, P, P, P, P]
         lib.oracle_topk.argtypes = [I, I, I, P, P, P, P]
+        lib.oracle_topk_ex.argtypes = [I, I, I, I, I, P, P, P, P]
         lib.oracle_capacity.argtypes = [LL, I, I, D]
         lib.oracle_capacity.restype = LL
         lib.oracle_dispatch.argtypes = [I, I, I, LL, P, P, P, P, P, P, P, P]
@@ -113,17 +114,21 @@ def router_logits(x, Wr, bias=None, tokens=None) -> np.ndarray:
     return out
 
 
-def topk(logits, k: int):
-    """Softmax over all experts, top-k on the logits (ties to the lower index),
-    renormalised kept weights.  "How Mixture of Experts Works", section "The
-    Gating Mechanism".  Returns (idx int32 [T,k], w float64 [T,k], probs
-    float64 [T,E])."""
+def topk(logits, k: int, scoring: str = "softmax", renorm: bool = True):
+    """Scores, top-k on the logits (ties to the lower index), kept weights.
+    Default: softmax over all experts and renormalised weights ("How Mixture
+    of Experts Works", section "The Gating Mechanism").  scoring="sigmoid"
+    scores each expert independently and renorm=False keeps the raw kept
+    scores ("Mixture-of-Experts routing", "The knobs").  Returns (idx int32
+    [T,k], w float64 [T,k], probs float64 [T,E] = the scores)."""
     l = np.ascontiguousarray(np.asarray(logits, dtype=np.float64))
     T, E = l.shape
     idx = np.empty((T, k), dtype=np.int32)
     w = np.empty((T, k), dtype=np.float64)
     probs = np.empty((T, E), dtype=np.float64)
-    _load().oracle_topk(T, E, k, _ptr(l), _ptr(idx), _ptr(w), _ptr(probs))
+    sc = 1 if scoring == "sigmoid" else 0
+    _load().oracle_topk_ex(T, E, k, sc, 1 if renorm else 0, _ptr(l), _ptr(idx), _ptr(w),
+                           _ptr(probs))
     return idx, w, probs
 
 
@@ -237,7 +242,7 @@ def layer_forward(inp, logits_in=None, tokens=None, want_slots=False, want_share
         logits = router_logits(inp["x"], inp["Wr"], inp.get("logit_bias"))
     else:
         logits = np.asarray(logits_in, dtype=np.float64)
-    idx, w, probs = topk(logits, k)
+    idx, w, probs = topk(logits, k, cfg.get("scoring", "softmax"), cfg.get("renorm", True))
     cap = capacity(T, k, E, cfg.get("capacity_factor", 0.0))
     disp = dispatch(idx, E, cap)
     toks = np.arange(T, dtype=np.int32) if tokens is None else np.asarray(tokens, np.int32)

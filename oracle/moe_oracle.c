@@ -56,6 +56,7 @@
 
 enum { ORC_F32 = 0, ORC_BF16 = 1 };
 enum { ORC_GELU_ERF = 0, ORC_SWIGLU = 1 };
+enum { ORC_SOFTMAX = 0, ORC_SIGMOID = 1 };
 
 /* Exact widening of one stored element to double.  bf16 is the upper half of
  * an IEEE binary32 pattern. */
@@ -161,30 +162,38 @@ void oracle_router_logits(int ntok, const int *tokens, int d, int E, int dtype,
     orc_parallel(ntok, orc_router_range, &c);
 }
 
-/* ------------------------------------- steps 2-4: softmax, top-k, renorm */
-/* probs[t,:] = softmax(logits[t,:]) over all E experts ([R], [G]).
- * top-k: experts ordered by logit descending, ties to the lower index; slot 0
- * holds the largest.  Weights: the kept probabilities divided by their sum
- * ([R] "Renormalize so selected weights sum to 1"). */
-void oracle_topk(int T, int E, int k, const double *logits, int *topk_idx,
-                 double *topk_w, double *probs)
+/* ------------------------------------- steps 2-4: scores, top-k, renorm */
+/* Scores ([R], [G]): softmax over all E experts, or (the variant the
+ * "Mixture-of-Experts routing" page names under "The knobs") an independent
+ * sigmoid per expert.  top-k: experts ordered by logit descending, ties to the
+ * lower index; slot 0 holds the largest (both score functions are monotone in
+ * the logit, so the order is the logits').  Weights: the kept scores divided
+ * by their sum ([R] "Renormalize so selected weights sum to 1"), or the kept
+ * scores as they are when renorm == 0.  probs receives the scores. */
+void oracle_topk_ex(int T, int E, int k, int scoring, int renorm, const double *logits,
+                    int *topk_idx, double *topk_w, double *probs)
 {
     unsigned char *taken = (unsigned char *)malloc((size_t)E);
     double *p = (double *)malloc(sizeof(double) * (size_t)E);
     for (int t = 0; t < T; ++t) {
         const double *l = logits + (size_t)t * E;
-        double m = l[0];
-        for (int e = 1; e < E; ++e)
-            if (l[e] > m)
-                m = l[e];
-        double Z = 0.0;
-        for (int e = 0; e < E; ++e)
-            Z += exp(l[e] - m);
-        for (int e = 0; e < E; ++e) {
-            p[e] = exp(l[e] - m) / Z;
-            if (probs)
-                probs[(size_t)t * E + e] = p[e];
+        if (scoring == ORC_SIGMOID) {
+            for (int e = 0; e < E; ++e)
+                p[e] = 1.0 / (1.0 + exp(-l[e]));
+        } else {
+            double m = l[0];
+            for (int e = 1; e < E; ++e)
+                if (l[e] > m)
+                    m = l[e];
+            double Z = 0.0;
+            for (int e = 0; e < E; ++e)
+                Z += exp(l[e] - m);
+            for (int e = 0; e < E; ++e)
+                p[e] = exp(l[e] - m) / Z;
         }
+        if (probs)
+            for (int e = 0; e < E; ++e)
+                probs[(size_t)t * E + e] = p[e];
         memset(taken, 0, (size_t)E);
         double kept = 0.0;
         for (int s = 0; s < k; ++s) {
@@ -196,11 +205,20 @@ void oracle_topk(int T, int E, int k, const double *logits, int *topk_idx,
             topk_idx[(size_t)t * k + s] = best;
             kept += p[best];
         }
-        for (int s = 0; s < k; ++s)
-            topk_w[(size_t)t * k + s] = p[topk_idx[(size_t)t * k + s]] / kept;
+        for (int s = 0; s < k; ++s) {
+            double w = p[topk_idx[(size_t)t * k + s]];
+            topk_w[(size_t)t * k + s] = renorm ? w / kept : w;
+        }
     }
     free(taken);
     free(p);
+}
+
+/* The pages' default router: softmax scores, renormalised kept weights. */
+void oracle_topk(int T, int E, int k, const double *logits, int *topk_idx,
+                 double *topk_w, double *probs)
+{
+    oracle_topk_ex(T, E, k, ORC_SOFTMAX, 1, logits, topk_idx, topk_w, probs);
 }
 
 /* ------------------------------------------------------- step 6: capacity */

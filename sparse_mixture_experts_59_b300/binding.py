@@ -15,6 +15,7 @@ LIB_PATH = os.path.join(_HERE, "libmoe_b300.so")
 
 MOE_F32, MOE_BF16 = 0, 1
 MOE_GELU_ERF, MOE_SWIGLU = 0, 1
+MOE_SCORE_SOFTMAX, MOE_SCORE_SIGMOID = 0, 1
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
           4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_TIMEOUT", 6: "MOE_ERR_DEVICE_BOUNDS",
           7: "MOE_ERR_NO_DEVICE"}
@@ -35,7 +36,8 @@ class MoeConfig(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int), ("d", ctypes.c_int), ("F", ctypes.c_int),
                 ("E", ctypes.c_int), ("k", ctypes.c_int), ("F_shared", ctypes.c_int),
                 ("dtype", ctypes.c_int), ("act", ctypes.c_int), ("has_bias", ctypes.c_int),
-                ("capacity_factor", ctypes.c_float)]
+                ("capacity_factor", ctypes.c_float), ("scoring", ctypes.c_int),
+                ("no_renorm", ctypes.c_int)]
 
 
 class MoeWeights(ctypes.Structure):
@@ -95,7 +97,9 @@ def make_config(cfg: dict) -> MoeConfig:
         dtype=MOE_F32 if cfg.get("dtype", "bf16") in ("f32", torch.float32) else MOE_BF16,
         act=MOE_SWIGLU if cfg.get("act", "swiglu") == "swiglu" else MOE_GELU_ERF,
         has_bias=int(bool(cfg.get("has_bias", False))),
-        capacity_factor=float(cfg.get("capacity_factor", 0.0) or 0.0))
+        capacity_factor=float(cfg.get("capacity_factor", 0.0) or 0.0),
+        scoring=MOE_SCORE_SIGMOID if cfg.get("scoring", "softmax") == "sigmoid" else MOE_SCORE_SOFTMAX,
+        no_renorm=0 if cfg.get("renorm", True) else 1)
 
 
 def _p(t):

@@ -94,6 +94,9 @@ int check_cfg(const moe_cfg* c) {
     if (c->F_shared > 0 && c->act != MOE_SWIGLU)
         return fail(MOE_ERR_UNSUPPORTED, "the shared expert is a SwiGLU expert; needs act = SwiGLU%s");
     if (!(c->capacity_factor == c->capacity_factor)) return fail(MOE_ERR_INVALID_ARG, "capacity_factor is NaN%s");
+    if (c->scoring != MOE_SCORE_SOFTMAX && c->scoring != MOE_SCORE_SIGMOID)
+        return fail(MOE_ERR_INVALID_ARG, "unknown scoring%s");
+    if (c->no_renorm != 0 && c->no_renorm != 1) return fail(MOE_ERR_INVALID_ARG, "no_renorm must be 0 or 1%s");
     return MOE_OK;
 }
 
@@ -259,7 +262,8 @@ int run_route(const moe_cfg& c, const DevInfo& di, const void* x, const void* Wr
         MOE_CUDA(launch_router_logits_simt(c.dtype, x, Wr, bias, logits, c.T, c.d, c.E, st),
                  "router logits launch");
     }
-    MOE_CUDA(launch_router_topk(part, nsplit, topk_bias, logits, c.T, c.E, c.k, topk_idx, topk_w,
+    MOE_CUDA(launch_router_topk(part, nsplit, topk_bias, logits, c.T, c.E, c.k, c.scoring,
+                                !c.no_renorm, topk_idx, topk_w,
                                 at<float>(ws, L.prob_part), prob_mean,
                                 at<int>(ws, L.ctrl) + kCtrlRouterDone, router_blocks(c.T), st),
              "router top-k launch");

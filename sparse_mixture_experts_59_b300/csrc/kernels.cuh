@@ -26,7 +26,8 @@ cudaError_t launch_router_logits_simt(int dtype, const void* x, const void* Wr, 
 // top-k reads nsplit partial-logit slabs part[s][T][E], adds them in order
 // and the bias, writes logits, then softmax / top-k / renormalise.
 cudaError_t launch_router_topk(const float* part, int nsplit, const float* bias, float* logits,
-                               int T, int E, int k, int* topk_idx, float* topk_w,
+                               int T, int E, int k, int scoring, int renorm, int* topk_idx,
+                               float* topk_w,
                                float* prob_part, float* prob_mean, int* done, int nblocks,
                                cudaStream_t st);
 

@@ -78,7 +78,7 @@ router_logits_simt(const T* __restrict__ x, const T* __restrict__ Wr,
 template <int VPL>
 __global__ void __launch_bounds__(256)
 router_topk_kernel(const float* part, int nsplit, const float* __restrict__ bias,
-                   float* logits, int Ttok, int E, int k,
+                   float* logits, int Ttok, int E, int k, int scoring, int renorm,
                    int* __restrict__ topk_idx, float* __restrict__ topk_w,
                    float* __restrict__ prob_part, float* __restrict__ prob_mean,
                    int* __restrict__ done_counter) {
@@ -113,17 +113,23 @@ router_topk_kernel(const float* part, int nsplit, const float* __restrict__ bias
         for (int j = 1; j < VPL; ++j) m = fmaxf(m, l[j]);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        // ex: exp(l - max) (softmax) or the sigmoid score itself; p = ex * inv
         float ex[VPL];
         float z = 0.f;
 #pragma unroll
         for (int j = 0; j < VPL; ++j) {
-            ex[j] = (lane + 32 * j < E) ? expf(l[j] - m) : 0.f;
+            const bool ok = lane + 32 * j < E;
+            ex[j] = !ok ? 0.f
+                  : scoring == MOE_SCORE_SIGMOID ? 1.f / (1.f + expf(-l[j])) : expf(l[j] - m);
             z += ex[j];
         }
+        float inv = 1.f;
+        if (scoring != MOE_SCORE_SIGMOID) {
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+            for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+            inv = 1.f / z;
+        }
         if (want_p) {
-            const float inv = 1.f / z;
 #pragma unroll
             for (int j = 0; j < VPL; ++j)
                 if (lane + 32 * j < E) s_psum[warp][lane + 32 * j] += ex[j] * inv;
@@ -162,7 +168,7 @@ router_topk_kernel(const float* part, int nsplit, const float* __restrict__ bias
         }
         if (lane < k) {
             topk_idx[(size_t)t * k + lane] = my_idx;
-            topk_w[(size_t)t * k + lane] = my_ex / kept_ex;
+            topk_w[(size_t)t * k + lane] = renorm ? my_ex / kept_ex : my_ex * inv;
         }
     }
     if (!want_p) return;
@@ -211,7 +217,8 @@ cudaError_t launch_router_logits_simt(int dtype, const void* x, const void* Wr, 
 }
 
 cudaError_t launch_router_topk(const float* part, int nsplit, const float* bias, float* logits,
-                               int T, int E, int k, int* topk_idx, float* topk_w,
+                               int T, int E, int k, int scoring, int renorm, int* topk_idx,
+                               float* topk_w,
                                float* prob_part, float* prob_mean, int* done, int nblocks,
                                cudaStream_t st) {
     const int vpl = (E + 31) / 32;
@@ -219,7 +226,7 @@ cudaError_t launch_router_topk(const float* part, int nsplit, const float* bias,
                 : vpl <= 2 ? router_topk_kernel<2>
                 : vpl <= 4 ? router_topk_kernel<4> : router_topk_kernel<8>;
     return launch_kernel(kernel, dim3(nblocks), dim3(256), 0, st, 1, part, nsplit, bias, logits, T,
-                         E, k, topk_idx, topk_w, prob_part, prob_mean, done);
+                         E, k, scoring, renorm, topk_idx, topk_w, prob_part, prob_mean, done);
 }
 
 }  // namespace moe

@@ -32,6 +32,12 @@ SMALL = {
                            capacity_factor=1.25, seed=2005),
     "swiglu_fp32_shared": dict(base="fine_grained", T=70, d=96, F=64, E=5, k=2, F_shared=48,
                                dtype="f32", seed=2006),
+    "sigmoid_shared_small": dict(base="fine_grained", T=160, d=192, F=128, E=16, k=4,
+                                 F_shared=128, scoring="sigmoid", seed=2007),
+    "softmax_norenorm_cap": dict(base="mixtral_prefill", T=400, d=256, F=384, E=8, k=2,
+                                 renorm=False, capacity_factor=1.0, seed=2008),
+    "sigmoid_fp32_norenorm": dict(base="tiny_fp32", T=90, scoring="sigmoid", renorm=False,
+                                  seed=2009),
 }
 
 

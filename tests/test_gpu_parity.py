@@ -63,7 +63,8 @@ def test_routing_indices_bit_exact(run):
 def test_gate_weights(run):
     g, r = run["gpu"], run["ref"]
     assert max_rel(f64(g["topk_w"]), r["topk_w"]) < TOL_W
-    np.testing.assert_allclose(f64(g["topk_w"]).sum(axis=1), 1.0, atol=1e-6)
+    if run["cfg"].get("renorm", True):
+        np.testing.assert_allclose(f64(g["topk_w"]).sum(axis=1), 1.0, atol=1e-6)
 
 
 def test_router_logits_against_own_oracle_logits(run):

@@ -352,3 +352,39 @@ def test_workload_capacities_and_skew():
     assert oracle.capacity(c4["T"], c4["k"], c4["E"], c4["capacity_factor"]) == 256
     b = workloads.skew_bias(64).numpy()
     np.testing.assert_allclose(b, -1.8 * np.log(np.arange(1, 65)), rtol=1e-6, atol=1e-6)
+
+
+# ------------------------------------------------------- scoring variants
+def test_sigmoid_scores_and_unrenormalised_weights():
+    """Sigmoid scoring gives scipy's expit of every logit; without
+    renormalisation the kept weights are the kept scores themselves; the
+    selected experts are those of the softmax router (both are monotone)."""
+    r = _rng(21)
+    logits = r.normal(scale=2.0, size=(300, 12))
+    k = 3
+    idx_soft, w_soft, p_soft = oracle.topk(logits, k)
+    idx_sig, w_sig, p_sig = oracle.topk(logits, k, scoring="sigmoid", renorm=True)
+    np.testing.assert_array_equal(idx_sig, idx_soft)
+    np.testing.assert_allclose(p_sig, expit(logits), rtol=1e-14, atol=0)
+    sel = np.take_along_axis(p_sig, idx_sig.astype(np.int64), axis=1)
+    np.testing.assert_allclose(w_sig, sel / sel.sum(axis=1, keepdims=True), rtol=1e-13)
+    _, w_raw, _ = oracle.topk(logits, k, scoring="sigmoid", renorm=False)
+    np.testing.assert_allclose(w_raw, sel, rtol=0, atol=0)
+    _, w_soft_raw, _ = oracle.topk(logits, k, scoring="softmax", renorm=False)
+    np.testing.assert_allclose(w_soft_raw, np.take_along_axis(p_soft, idx_soft.astype(np.int64), axis=1),
+                               rtol=0, atol=0)
+    # unrenormalised softmax weights sum to less than one unless k = E
+    assert np.all(w_soft_raw.sum(axis=1) < 1.0)
+
+
+def test_sigmoid_layer_single_expert_is_scaled_dense_ffn():
+    """E=1, k=1 with sigmoid scoring and no renormalisation: y = x +
+    sigmoid(l) * FFN(x) (numpy)."""
+    inp = _small_inputs("swiglu", E=1, k=1, seed=22)
+    inp["cfg"]["scoring"] = "sigmoid"
+    inp["cfg"]["renorm"] = False
+    out = oracle.layer_forward(inp)
+    l = inp["x"].astype(np.float64) @ inp["Wr"].astype(np.float64).T
+    ref = _np_ffn(inp["x"], inp["W1"][0], inp["W3"][0], inp["W2"][0], None, None, "swiglu")
+    np.testing.assert_allclose(out["y"], inp["x"].astype(np.float64) + expit(l) * ref,
+                               rtol=1e-12, atol=1e-12)
