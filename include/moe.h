@@ -211,6 +211,21 @@ int moe_layer_forward(const moe_cfg *cfg, const void *x, const void *Wr, const f
                       const moe_weights *w, const moe_layer_out *out,
                       void *ws, size_t ws_bytes, void *stream);
 
+/* Backward of the aux loss through the router (training; "How Mixture of
+ * Experts Works", "The Load Balancing Problem": the loss adds alpha * aux).
+ * f_e = counts_pre[e]/T is piecewise constant and carries no gradient; with
+ * g = grad_aux = dLoss/daux and p the router scores of cfg->scoring:
+ *   softmax: grad_logits[t,j] = g (E/T) p[t,j] (f_j - sum_e f_e p[t,e])
+ *   sigmoid: grad_logits[t,j] = g (E/T) f_j p[t,j] (1 - p[t,j])
+ *   grad_Wr[e,i] = sum_t grad_logits[t,e] x[t,i]       (optional, may be NULL)
+ *   grad_x[t,i]  = sum_e grad_logits[t,e] Wr[e,i]       (optional, may be NULL)
+ * logits [T,E] fp32 and counts_pre [E] are moe_route / moe_dispatch outputs;
+ * x [T,d], Wr [E,d] in the layer dtype; all gradients fp32, accumulated in
+ * fp32 on CUDA cores. */
+int moe_aux_loss_backward(const moe_cfg *cfg, const void *x, const void *Wr, const float *logits,
+                          const int *counts_pre, float grad_aux, float *grad_logits,
+                          float *grad_Wr, float *grad_x, void *stream);
+
 /* moe_layer_forward that also records seven caller-created CUDA events
  * (cudaEvent_t handles, created with timing enabled) on `stream` at the stage
  * boundaries, so a caller can time each kernel on the stream it runs on:

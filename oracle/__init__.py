@@ -38,6 +38,7 @@ def _load():
                                             I, P, P, P, P, P, P, P, P, P]
         lib.oracle_aux_loss.argtypes = [I, I, P, P]
         lib.oracle_aux_loss.restype = D
+        lib.oracle_aux_grad_logits.argtypes = [I, I, I, P, P, D, P]
         lib.oracle_set_threads.argtypes = [I]
         lib.oracle_get_threads.restype = I
         _lib = lib
@@ -252,3 +253,27 @@ def layer_forward(inp, logits_in=None, tokens=None, want_slots=False, want_share
     A = T * k
     out["drop_frac"] = (A - disp["R"]) / A if A else 0.0
     return out
+
+
+def aux_grad_logits(logits, counts_pre, grad_aux=1.0, scoring="softmax"):
+    """Gradient of grad_aux * aux with respect to the router logits, f_e held
+    fixed (counts are piecewise constant): the chain rule through P_e, see
+    oracle_aux_grad_logits.  "How Mixture of Experts Works", "The Load
+    Balancing Problem" (the aux term is trained as alpha * aux)."""
+    l = np.ascontiguousarray(np.asarray(logits, dtype=np.float64))
+    T, E = l.shape
+    cp = np.ascontiguousarray(np.asarray(counts_pre, dtype=np.int32))
+    g = np.empty((T, E), np.float64)
+    _load().oracle_aux_grad_logits(T, E, 1 if scoring == "sigmoid" else 0, _ptr(l), _ptr(cp),
+                                   float(grad_aux), _ptr(g))
+    return g
+
+
+def aux_router_backward(x, Wr, logits, counts_pre, grad_aux=1.0, scoring="softmax"):
+    """Router gradients of grad_aux * aux: (g_logits [T,E], g_Wr [E,d] =
+    g_logits^T x, g_x [T,d] = g_logits Wr), in double; the two products are
+    library matmuls of the exactly widened inputs."""
+    g = aux_grad_logits(logits, counts_pre, grad_aux, scoring)
+    xf = to_f64(x)
+    wf = to_f64(Wr)
+    return g, g.T @ xf, g @ wf

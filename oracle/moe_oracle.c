@@ -419,3 +419,52 @@ double oracle_aux_loss(int T, int E, const int *counts_pre, const double *probs)
     }
     return (double)E * aux;
 }
+
+/* ------------------------------------------- aux loss backward (router) */
+/* The aux term enters the training loss as alpha * aux ("How Mixture of
+ * Experts Works", "The Load Balancing Problem").  f_e = counts_pre[e] / T is
+ * piecewise constant in the logits and carries no gradient; P_e = mean_t
+ * p[t,e] does.  With g = grad_aux (dLoss/daux):
+ *   d aux / d p[t,e] = E f_e / T
+ *   softmax: d p[t,e] / d l[t,j] = p[t,e] (delta_ej - p[t,j])
+ *            => g_l[t,j] = g (E/T) p[t,j] (f_j - sum_e f_e p[t,e])
+ *   sigmoid: d p[t,e] / d l[t,e] = p[t,e] (1 - p[t,e])
+ *            => g_l[t,j] = g (E/T) f_j p[t,j] (1 - p[t,j])
+ * Each term is written out as the chain rule gives it. */
+void oracle_aux_grad_logits(int T, int E, int scoring, const double *logits,
+                            const int *counts_pre, double grad_aux, double *g_l)
+{
+    double *p = (double *)malloc(sizeof(double) * (size_t)E);
+    double *dp = (double *)malloc(sizeof(double) * (size_t)E);
+    for (int t = 0; t < T; ++t) {
+        const double *l = logits + (size_t)t * E;
+        if (scoring == ORC_SIGMOID) {
+            for (int e = 0; e < E; ++e)
+                p[e] = 1.0 / (1.0 + exp(-l[e]));
+        } else {
+            double m = l[0];
+            for (int e = 1; e < E; ++e)
+                if (l[e] > m)
+                    m = l[e];
+            double Z = 0.0;
+            for (int e = 0; e < E; ++e)
+                Z += exp(l[e] - m);
+            for (int e = 0; e < E; ++e)
+                p[e] = exp(l[e] - m) / Z;
+        }
+        for (int e = 0; e < E; ++e) /* d aux / d p[t,e] */
+            dp[e] = grad_aux * (double)E * ((double)counts_pre[e] / (double)T) / (double)T;
+        for (int j = 0; j < E; ++j) {
+            double acc = 0.0;
+            if (scoring == ORC_SIGMOID) {
+                acc = dp[j] * p[j] * (1.0 - p[j]);
+            } else {
+                for (int e = 0; e < E; ++e)
+                    acc += dp[e] * p[e] * ((e == j ? 1.0 : 0.0) - p[j]);
+            }
+            g_l[(size_t)t * E + j] = acc;
+        }
+    }
+    free(p);
+    free(dp);
+}

@@ -22,7 +22,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 EXPORTS = ("moe_status_string", "moe_last_error", "moe_capacity", "moe_workspace_size",
            "moe_workspace_init", "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine",
            "moe_layer_forward", "moe_layer_forward_profiled", "moe_get_device_status",
-           "moe_dispatch_noalloc", "moe_test_hold_lookback_block")
+           "moe_dispatch_noalloc", "moe_test_hold_lookback_block", "moe_aux_loss_backward")
 
 
 class MoeError(RuntimeError):
@@ -78,6 +78,7 @@ def lib():
         L.moe_get_device_status.argtypes = [P, S, P, ctypes.POINTER(I)]
         L.moe_dispatch_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P]
         L.moe_test_hold_lookback_block.argtypes = [P, S, I, P]
+        L.moe_aux_loss_backward.argtypes = [P, P, P, P, P, ctypes.c_float, P, P, P, P]
         for name in EXPORTS:
             getattr(L, name).restype = getattr(L, name).restype or I
         _lib = L
@@ -258,6 +259,22 @@ def layer_forward(cfg, x, Wr, weights: dict, logit_bias=None, ws=None, outputs=N
                                                 ctypes.byref(w), ctypes.byref(out_s), _p(ws),
                                                 ws.numel(), _stream(stream), ev))
     return o
+
+
+def aux_loss_backward(cfg, x, Wr, logits, counts_pre, grad_aux=1.0, want_Wr=True, want_x=True,
+                      stream=None):
+    """moe_aux_loss_backward: router gradients of grad_aux * aux.  Returns
+    dict(grad_logits [T,E], grad_Wr [E,d] or None, grad_x [T,d] or None),
+    all fp32."""
+    c = cfg if isinstance(cfg, MoeConfig) else make_config(cfg)
+    dev = logits.device
+    out = dict(grad_logits=torch.empty(c.T, c.E, dtype=torch.float32, device=dev),
+               grad_Wr=torch.empty(c.E, c.d, dtype=torch.float32, device=dev) if want_Wr else None,
+               grad_x=torch.empty(c.T, c.d, dtype=torch.float32, device=dev) if want_x else None)
+    _check(lib().moe_aux_loss_backward(ctypes.byref(c), _p(x), _p(Wr), _p(logits), _p(counts_pre),
+                                       float(grad_aux), _p(out["grad_logits"]), _p(out["grad_Wr"]),
+                                       _p(out["grad_x"]), _stream(stream)))
+    return out
 
 
 def test_hold_lookback_block(ws, block, stream=None):

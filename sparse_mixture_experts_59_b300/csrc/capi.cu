@@ -596,6 +596,31 @@ int moe_layer_forward_profiled(const moe_cfg* cfg, const void* x, const void* Wr
     return layer_forward_impl(cfg, x, Wr, logit_bias, w, out, ws, ws_bytes, stream, events);
 }
 
+int moe_aux_loss_backward(const moe_cfg* cfg, const void* x, const void* Wr, const float* logits,
+                          const int* counts_pre, float grad_aux, float* grad_logits,
+                          float* grad_Wr, float* grad_x, void* stream) {
+    MOE_TRY(check_cfg(cfg));
+    if (cfg->T == 0) return MOE_OK;
+    MOE_TRY(check_ptr4(logits, "logits"));
+    MOE_TRY(check_ptr4(counts_pre, "counts_pre"));
+    MOE_TRY(check_ptr4(grad_logits, "grad_logits"));
+    if (grad_Wr) {
+        MOE_TRY(check_ptr(x, "x"));
+        MOE_TRY(check_ptr4(grad_Wr, "grad_Wr"));
+    }
+    if (grad_x) {
+        MOE_TRY(check_ptr(Wr, "Wr"));
+        MOE_TRY(check_ptr4(grad_x, "grad_x"));
+    }
+    DevInfo di;
+    MOE_TRY(device_info(&di));
+    MOE_CUDA(launch_aux_backward(cfg->dtype, cfg->scoring, x, Wr, logits, counts_pre, grad_aux,
+                                 cfg->T, cfg->d, cfg->E, grad_logits, grad_Wr, grad_x, di.num_sms,
+                                 (cudaStream_t)stream),
+             "aux backward launch");
+    return MOE_OK;
+}
+
 int moe_test_hold_lookback_block(void* ws, size_t ws_bytes, int block, void* stream) {
     if (!ws) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL%s");
     if (ws_bytes < kCtrlWords * 4) return fail(MOE_ERR_WORKSPACE, "workspace too small%s");

@@ -42,6 +42,12 @@ RouterPlan router_tc_plan(int T, int d, int E);
 cudaError_t launch_router_tc(const CUtensorMap& map_x, const CUtensorMap& map_w, int T, int E,
                              const RouterPlan& p, float* part, int* status, cudaStream_t st);
 
+// aux_backward.cu (router gradients of the aux loss)
+cudaError_t launch_aux_backward(int dtype, int scoring, const void* x, const void* Wr,
+                                const float* logits, const int* counts_pre, float grad_aux, int T,
+                                int d, int E, float* g_l, float* g_Wr, float* g_x, int num_sms,
+                                cudaStream_t st);
+
 // dispatch.cu
 cudaError_t launch_dispatch(const int* topk_idx, int T, int k, int E, long long cap,
                             unsigned* tile_status, int* ctrl, int* rank, int* counts_pre,

@@ -388,3 +388,42 @@ def test_sigmoid_layer_single_expert_is_scaled_dense_ffn():
     ref = _np_ffn(inp["x"], inp["W1"][0], inp["W3"][0], inp["W2"][0], None, None, "swiglu")
     np.testing.assert_allclose(out["y"], inp["x"].astype(np.float64) + expit(l) * ref,
                                rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------ aux loss backward
+@pytest.mark.parametrize("scoring", ["softmax", "sigmoid"])
+def test_aux_gradient_matches_central_differences(scoring):
+    """The analytic logit gradient of the aux loss equals central finite
+    differences of the oracle's own aux loss with the counts held fixed."""
+    r = _rng(31)
+    T, E, k = 6, 5, 2
+    logits = r.normal(size=(T, E))
+    idx, _, probs = oracle.topk(logits, k, scoring=scoring)
+    counts = oracle.dispatch(idx, E, -1)["counts_pre"]
+    g = oracle.aux_grad_logits(logits, counts, grad_aux=0.7, scoring=scoring)
+    h = 1e-6
+    for t in range(T):
+        for j in range(E):
+            lp, lm = logits.copy(), logits.copy()
+            lp[t, j] += h
+            lm[t, j] -= h
+            ap = oracle.aux_loss(counts, oracle.topk(lp, k, scoring=scoring)[2])
+            am = oracle.aux_loss(counts, oracle.topk(lm, k, scoring=scoring)[2])
+            assert g[t, j] == pytest.approx(0.7 * (ap - am) / (2 * h), rel=1e-6, abs=1e-10)
+
+
+def test_aux_router_backward_products():
+    """g_Wr = g^T x and g_x = g Wr (numpy matmuls), with x, Wr in nn.Linear
+    layout; softmax rows of the logit gradient sum to zero."""
+    r = _rng(32)
+    T, d, E = 9, 7, 4
+    x = r.normal(size=(T, d)).astype(np.float32)
+    Wr = r.normal(size=(E, d)).astype(np.float32)
+    logits = oracle.router_logits(x, Wr)
+    idx, _, _ = oracle.topk(logits, 2)
+    counts = oracle.dispatch(idx, E, -1)["counts_pre"]
+    g, gW, gx = oracle.aux_router_backward(x, Wr, logits, counts)
+    np.testing.assert_allclose(g.sum(axis=1), 0.0, atol=1e-15)
+    np.testing.assert_allclose(gW, g.T @ x.astype(np.float64), rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(gx, g @ Wr.astype(np.float64), rtol=1e-12, atol=1e-15)
+    assert gW.shape == (E, d) and gx.shape == (T, d)
