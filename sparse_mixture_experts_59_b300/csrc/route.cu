@@ -192,8 +192,15 @@ router_topk_kernel(const float* part, int nsplit, const float* __restrict__ bias
     float* s_col = &s_psum[0][0];                  // reuse: [G][E] partial columns
     if ((int)threadIdx.x < G * E) {
         const int e = threadIdx.x % E, g = threadIdx.x / E;
+        float a8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // 8 loads in flight
+        int b = g;
+        for (; b + 7 * G < (int)gridDim.x; b += 8 * G)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) a8[j] += __ldcg(prob_part + (size_t)(b + j * G) * E + e);
+        for (; b < (int)gridDim.x; b += G) a8[0] += __ldcg(prob_part + (size_t)b * E + e);
         float acc = 0.f;
-        for (int b = g; b < (int)gridDim.x; b += G) acc += __ldcg(prob_part + (size_t)b * E + e);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc += a8[j];
         s_col[g * E + e] = acc;
     }
     __syncthreads();
