@@ -331,6 +331,7 @@ def run_ours(args, world, rank, local):
         result["e2e"] = run_e2e(layer, cfg, x, args, world, dev)
     if not args.no_decode:
         result["decode"] = run_decode(args, inp, world, dev, peaks, peak_src)
+        result["decode_fp8"] = run_decode(args, inp, world, dev, peaks, peak_src, fp8=True)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(inp, cfg, args.cpu_seconds)
     del layer
@@ -367,13 +368,17 @@ def run_e2e(layer, cfg, x, args, world, dev):
             "steps": steps}
 
 
-def run_decode(args, prefill_inp, world, dev, peaks, peak_src):
+def run_decode(args, prefill_inp, world, dev, peaks, peak_src, fp8=False):
     """Decode-shaped layer (T=32) on the same expert weights: weight streaming
-    of the experts that got tokens, against the HBM roofline."""
+    of the experts that got tokens, against the HBM roofline.  fp8=True: the
+    same weights quantised to E4M3 with per-row scales (half the bytes)."""
     cfg = workloads.config(args.decode_workload)
     inp = dict(prefill_inp)
     inp["x"] = workloads.make_x(cfg, dev)
     inp["cfg"] = cfg
+    if fp8:
+        inp = workloads.quantize_experts_fp8(inp)
+        cfg = inp["cfg"]
     layer = binding.MoeLayer(cfg, inp, device=dev)
     outputs = {"y": torch.empty_like(inp["x"]),
                "counts_kept": torch.empty(cfg["E"], dtype=torch.int32, device=dev)}
@@ -382,13 +387,14 @@ def run_decode(args, prefill_inp, world, dev, peaks, peak_src):
     ms = max_over_ranks(ms, world)
     counts = outputs["counts_kept"].cpu().numpy()
     hit = int((counts > 0).sum())
-    per_expert = 3 * cfg["d"] * cfg["F"] * 2
+    per_expert = 3 * cfg["d"] * cfg["F"] * (1 if fp8 else 2) + (2 * cfg["F"] + cfg["d"]) * 4 * fp8
     wbytes = hit * per_expert
     gemm_s = (stages["up_gemm"] + stages["down_gemm"]) / 1e3
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     gbs = wbytes / gemm_s / 1e9
     del layer
-    return {"workload": args.decode_workload, "T": cfg["T"], "experts_hit": hit,
+    return {"workload": args.decode_workload + (" (FP8 E4M3 expert weights)" if fp8 else ""),
+            "T": cfg["T"], "experts_hit": hit,
             "tokens_per_s": round(cfg["T"] * world / (ms / 1e3), 1), "ms_per_step": round(ms, 4),
             "weight_bytes": wbytes, "gemm_ms": round(gemm_s * 1e3, 4),
             "hbm_gbs": round(gbs, 1), "hbm_peak_gbs": hbm, "frac_of_hbm": round(gbs / hbm, 4),

@@ -92,6 +92,12 @@ enum moe_scoring { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 };
  *           ("Mixture-of-Experts routing", "The knobs": scoring_func)
  *  no_renorm 0 (default): kept scores divided by their sum; 1: kept scores
  *           used as they are (the same page's norm_topk_prob = false)
+ *  weight_fp8 0 (default): expert weights in the layer dtype; 1: routed expert
+ *           weights W1, W3, W2 are FP8 E4M3 codes (one byte each, same shapes)
+ *           with fp32 scales per output row in moe_weights.s1, s3, s2, i.e.
+ *           row i of W1 is s1[i] * W1[i,:] ("How Mixture of Experts Works",
+ *           "Quantization for MoE").  bf16 layers without a shared expert;
+ *           d and F multiples of 16.
  * A zero-filled moe_cfg with the sizes set gives the pages' default router. */
 typedef struct moe_cfg {
     int T, d, F, E, k;
@@ -102,14 +108,17 @@ typedef struct moe_cfg {
     float capacity_factor;
     int scoring;
     int no_renorm;
+    int weight_fp8;
 } moe_cfg;
 
 /* Expert weights (device pointers, dtype of the layer).  W3 only for SwiGLU;
- * b1, b2 only with has_bias; S1, S3, S2 only with F_shared > 0. */
+ * b1, b2 only with has_bias; S1, S3, S2 only with F_shared > 0; s1 [E,F],
+ * s3 [E,F], s2 [E,d] (fp32 row scales) only with weight_fp8. */
 typedef struct moe_weights {
     const void *W1, *W3, *W2;
     const void *b1, *b2;
     const void *S1, *S3, *S2;
+    const float *s1, *s3, *s2;
 } moe_weights;
 
 /* Outputs of moe_layer_forward.  y is required; every other pointer may be

@@ -14,7 +14,7 @@ import numpy as np
 
 from . import build as _build
 
-ORC_F32, ORC_BF16 = 0, 1
+ORC_F32, ORC_BF16, ORC_E4M3 = 0, 1, 2
 ORC_GELU_ERF, ORC_SWIGLU = 0, 1
 
 _lib = None
@@ -36,6 +36,10 @@ def _load():
         lib.oracle_expert_ffn.argtypes = [I, I, I, I, P, P, P, P, P, P, P, P]
         lib.oracle_layer_tokens.argtypes = [I, P, I, I, I, I, I, I, P, P, P, P, P, P,
                                             I, P, P, P, P, P, P, P, P, P]
+        lib.oracle_layer_tokens_q.argtypes = [I, P, I, I, I, I, I, I, I, P, P, P, P, P, P,
+                                              P, P, P, I, P, P, P, P, P, P, P, P, P]
+        lib.oracle_e4m3_value.argtypes = [ctypes.c_uint]
+        lib.oracle_e4m3_value.restype = D
         lib.oracle_aux_loss.argtypes = [I, I, P, P]
         lib.oracle_aux_loss.restype = D
         lib.oracle_aux_grad_logits.argtypes = [I, I, I, P, P, D, P]
@@ -69,6 +73,8 @@ def _buf(a):
                 return np.ascontiguousarray(a.view(torch.int16).numpy().view(np.uint16)), ORC_BF16
             if a.dtype == torch.float32:
                 return np.ascontiguousarray(a.numpy()), ORC_F32
+            if a.dtype == torch.float8_e4m3fn:
+                return np.ascontiguousarray(a.view(torch.uint8).numpy()), ORC_E4M3
             raise TypeError("oracle takes float32 or bfloat16 tensors, got %s" % a.dtype)
     except ImportError:
         pass
@@ -82,6 +88,12 @@ def _buf(a):
 
 def _ptr(a):
     return None if a is None else ctypes.c_void_p(a.ctypes.data)
+
+
+def e4m3_value(code: int) -> float:
+    """The oracle's decoding of one E4M3 byte (its own, from the format's
+    definition)."""
+    return float(_load().oracle_e4m3_value(int(code)))
 
 
 def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
@@ -190,7 +202,7 @@ def layer_tokens(inp, topk_idx, topk_w, drop_mask, tokens, want_slots=False,
     [n,d]."""
     cfg = inp["cfg"]
     xa, c = _buf(inp["x"])
-    W1, _ = _buf(inp["W1"])
+    W1, wc = _buf(inp["W1"])
     W3, _ = _buf(inp.get("W3"))
     W2, _ = _buf(inp["W2"])
     b1, _ = _buf(inp.get("b1"))
@@ -198,6 +210,19 @@ def layer_tokens(inp, topk_idx, topk_w, drop_mask, tokens, want_slots=False,
     S1, _ = _buf(inp.get("S1"))
     S3, _ = _buf(inp.get("S3"))
     S2, _ = _buf(inp.get("S2"))
+    scales = []
+    for key in ("s1", "s3", "s2"):
+        v = inp.get(key)
+        if v is not None and wc == ORC_E4M3:
+            try:
+                import torch
+                if isinstance(v, torch.Tensor):
+                    v = v.detach().cpu().float().numpy()
+            except ImportError:
+                pass
+            scales.append(np.ascontiguousarray(np.asarray(v, dtype=np.float32)))
+        else:
+            scales.append(None)
     tok = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
     n = len(tok)
     d, F, E, k = cfg["d"], cfg["F"], cfg["E"], cfg["k"]
@@ -209,9 +234,11 @@ def layer_tokens(inp, topk_idx, topk_w, drop_mask, tokens, want_slots=False,
     slots = np.empty((n, k, d), np.float64) if want_slots else None
     sh = np.empty((n, d), np.float64) if (want_shared and F_sh > 0) else None
     act = ORC_SWIGLU if cfg["act"] == "swiglu" else ORC_GELU_ERF
-    _load().oracle_layer_tokens(n, _ptr(tok), d, F, E, k, act, c, _ptr(xa), _ptr(W1), _ptr(W3),
-                                _ptr(W2), _ptr(b1), _ptr(b2), F_sh, _ptr(S1), _ptr(S3), _ptr(S2),
-                                _ptr(idx), _ptr(w), _ptr(dm), _ptr(y), _ptr(slots), _ptr(sh))
+    _load().oracle_layer_tokens_q(n, _ptr(tok), d, F, E, k, act, c, wc, _ptr(xa), _ptr(W1),
+                                  _ptr(W3), _ptr(W2), _ptr(b1), _ptr(b2), _ptr(scales[0]),
+                                  _ptr(scales[1]), _ptr(scales[2]), F_sh, _ptr(S1), _ptr(S3),
+                                  _ptr(S2), _ptr(idx), _ptr(w), _ptr(dm), _ptr(y), _ptr(slots),
+                                  _ptr(sh))
     out = {"y": y}
     if slots is not None:
         out["slots"] = slots

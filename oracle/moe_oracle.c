@@ -54,9 +54,25 @@
 #include <string.h>
 #include <unistd.h>
 
-enum { ORC_F32 = 0, ORC_BF16 = 1 };
+enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_E4M3 = 2 };
 enum { ORC_GELU_ERF = 0, ORC_SWIGLU = 1 };
 enum { ORC_SOFTMAX = 0, ORC_SIGMOID = 1 };
+
+/* E4M3 (FP8, 1 sign, 4 exponent bits with bias 7, 3 mantissa bits): normal
+ * codes are (-1)^s 2^(e-7) (1 + m/8); e = 0 gives the subnormals
+ * (-1)^s 2^-6 (m/8); e = 15, m = 7 is NaN (the format has no infinities). */
+double oracle_e4m3_value(unsigned code)
+{
+    const int sgn = (code >> 7) & 1, e = (code >> 3) & 15, m = code & 7;
+    double v;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m / 8.0, -6);
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sgn ? -v : v;
+}
 
 /* Exact widening of one stored element to double.  bf16 is the upper half of
  * an IEEE binary32 pattern. */
@@ -64,6 +80,8 @@ static double orc_load(const void *base, size_t i, int dtype)
 {
     if (dtype == ORC_F32)
         return (double)((const float *)base)[i];
+    if (dtype == ORC_E4M3)
+        return oracle_e4m3_value(((const unsigned char *)base)[i]);
     uint32_t bits = ((uint32_t)((const uint16_t *)base)[i]) << 16;
     float f;
     memcpy(&f, &bits, sizeof f);
@@ -280,41 +298,59 @@ int oracle_dispatch(int T, int k, int E, long long cap, const int *topk_idx,
  * SwiGLU ([S]): out = W2 . (silu(W1 . x) * (W3 . x)), silu(z) = z/(1+exp(-z)).
  * W1, W3 hold one row of d per hidden unit ([F, d]); W2 holds one row of F per
  * output ([d, F]) -- the nn.Linear weight layout.  b1 [F], b2 [d] optional.
- * h is caller scratch of F doubles. */
-void oracle_expert_ffn(int d, int F, int act, int dtype, const double *xv,
-                       const void *W1, const void *W3, const void *W2,
-                       const void *b1, const void *b2, double *h, double *out)
+ * Weights are stored in wdtype, biases in bdtype.  With E4M3 weights, s1, s3
+ * [F] and s2 [d] are the per-row scales: row f of W1 is s1[f] * W1[f,:]
+ * ("How Mixture of Experts Works", "Quantization for MoE"); each row's scale
+ * multiplies its dot product.  h is caller scratch of F doubles. */
+void oracle_expert_ffn_q(int d, int F, int act, int wdtype, int bdtype, const double *xv,
+                         const void *W1, const void *W3, const void *W2, const void *b1,
+                         const void *b2, const float *s1, const float *s3, const float *s2,
+                         double *h, double *out)
 {
     for (int f = 0; f < F; ++f) {
         double g = 0.0;
         for (int i = 0; i < d; ++i)
-            g += xv[i] * orc_load(W1, (size_t)f * d + i, dtype);
+            g += xv[i] * orc_load(W1, (size_t)f * d + i, wdtype);
+        if (s1)
+            g *= (double)s1[f];
         if (act == ORC_SWIGLU) {
             double u = 0.0;
             for (int i = 0; i < d; ++i)
-                u += xv[i] * orc_load(W3, (size_t)f * d + i, dtype);
+                u += xv[i] * orc_load(W3, (size_t)f * d + i, wdtype);
+            if (s3)
+                u *= (double)s3[f];
             h[f] = g / (1.0 + exp(-g)) * u;
         } else {
             if (b1)
-                g += orc_load(b1, (size_t)f, dtype);
+                g += orc_load(b1, (size_t)f, bdtype);
             h[f] = 0.5 * g * (1.0 + erf(g / sqrt(2.0)));
         }
     }
     for (int j = 0; j < d; ++j) {
         double o = 0.0;
         for (int f = 0; f < F; ++f)
-            o += h[f] * orc_load(W2, (size_t)j * F + f, dtype);
+            o += h[f] * orc_load(W2, (size_t)j * F + f, wdtype);
+        if (s2)
+            o *= (double)s2[j];
         if (b2)
-            o += orc_load(b2, (size_t)j, dtype);
+            o += orc_load(b2, (size_t)j, bdtype);
         out[j] = o;
     }
 }
 
+void oracle_expert_ffn(int d, int F, int act, int dtype, const double *xv,
+                       const void *W1, const void *W3, const void *W2,
+                       const void *b1, const void *b2, double *h, double *out)
+{
+    oracle_expert_ffn_q(d, F, act, dtype, dtype, xv, W1, W3, W2, b1, b2, NULL, NULL, NULL, h, out);
+}
+
 /* ------------------------------------------- step 9: layer output per token */
 typedef struct {
-    int d, F, E, k, act, dtype;
+    int d, F, E, k, act, dtype, wdtype;
     const void *x;
     const void *W1, *W3, *W2, *b1, *b2; /* [E,F,d], [E,F,d], [E,d,F], [E,F], [E,d] */
+    const float *s1, *s3, *s2;          /* E4M3 row scales [E,F], [E,F], [E,d] or NULL */
     int F_sh;
     const void *S1, *S3, *S2; /* shared expert [F_sh,d], [F_sh,d], [d,F_sh] */
     const int *topk_idx;
@@ -350,13 +386,17 @@ static void orc_layer_range(void *p, long lo, long hi)
             }
             int e = c->topk_idx[a];
             size_t wo = (size_t)e * F * d;
-            oracle_expert_ffn(d, F, c->act, c->dtype, xv,
-                              (const char *)c->W1 + wo * (c->dtype == ORC_F32 ? 4 : 2),
-                              c->W3 ? (const char *)c->W3 + wo * (c->dtype == ORC_F32 ? 4 : 2) : NULL,
-                              (const char *)c->W2 + wo * (c->dtype == ORC_F32 ? 4 : 2),
-                              c->b1 ? (const char *)c->b1 + (size_t)e * F * (c->dtype == ORC_F32 ? 4 : 2) : NULL,
-                              c->b2 ? (const char *)c->b2 + (size_t)e * d * (c->dtype == ORC_F32 ? 4 : 2) : NULL,
-                              h, tmp);
+            size_t we = c->wdtype == ORC_F32 ? 4 : c->wdtype == ORC_BF16 ? 2 : 1;
+            size_t be = c->dtype == ORC_F32 ? 4 : 2;
+            oracle_expert_ffn_q(d, F, c->act, c->wdtype, c->dtype, xv,
+                                (const char *)c->W1 + wo * we,
+                                c->W3 ? (const char *)c->W3 + wo * we : NULL,
+                                (const char *)c->W2 + wo * we,
+                                c->b1 ? (const char *)c->b1 + (size_t)e * F * be : NULL,
+                                c->b2 ? (const char *)c->b2 + (size_t)e * d * be : NULL,
+                                c->s1 ? c->s1 + (size_t)e * F : NULL,
+                                c->s3 ? c->s3 + (size_t)e * F : NULL,
+                                c->s2 ? c->s2 + (size_t)e * d : NULL, h, tmp);
             double w = c->topk_w[a];
             for (int i = 0; i < d; ++i) {
                 acc[i] += w * tmp[i];
@@ -386,6 +426,25 @@ static void orc_layer_range(void *p, long lo, long hi)
  * and the drop mask.  slots (optional, [ntok,k,d]) receives w * FFN_e(x) per
  * slot (zero when dropped); shared_out (optional, [ntok,d]) the shared
  * expert's output.  F_sh = 0 means no shared expert. */
+void oracle_layer_tokens_q(int ntok, const int *tokens, int d, int F, int E, int k,
+                           int act, int dtype, int wdtype, const void *x, const void *W1,
+                           const void *W3, const void *W2, const void *b1,
+                           const void *b2, const float *s1, const float *s3, const float *s2,
+                           int F_sh, const void *S1, const void *S3,
+                           const void *S2, const int *topk_idx, const double *topk_w,
+                           const unsigned char *drop_mask, double *y, double *slots,
+                           double *shared_out)
+{
+    orc_layer_ctx c;
+    c.d = d; c.F = F; c.E = E; c.k = k; c.act = act; c.dtype = dtype; c.wdtype = wdtype;
+    c.s1 = s1; c.s3 = s3; c.s2 = s2;
+    c.x = x; c.W1 = W1; c.W3 = W3; c.W2 = W2; c.b1 = b1; c.b2 = b2;
+    c.F_sh = F_sh; c.S1 = F_sh > 0 ? S1 : NULL; c.S3 = S3; c.S2 = S2;
+    c.topk_idx = topk_idx; c.topk_w = topk_w; c.drop_mask = drop_mask;
+    c.tokens = tokens; c.y = y; c.slots = slots; c.shared_out = shared_out;
+    orc_parallel(ntok, orc_layer_range, &c);
+}
+
 void oracle_layer_tokens(int ntok, const int *tokens, int d, int F, int E, int k,
                          int act, int dtype, const void *x, const void *W1,
                          const void *W3, const void *W2, const void *b1,
@@ -394,13 +453,9 @@ void oracle_layer_tokens(int ntok, const int *tokens, int d, int F, int E, int k
                          const unsigned char *drop_mask, double *y, double *slots,
                          double *shared_out)
 {
-    orc_layer_ctx c;
-    c.d = d; c.F = F; c.E = E; c.k = k; c.act = act; c.dtype = dtype;
-    c.x = x; c.W1 = W1; c.W3 = W3; c.W2 = W2; c.b1 = b1; c.b2 = b2;
-    c.F_sh = F_sh; c.S1 = F_sh > 0 ? S1 : NULL; c.S3 = S3; c.S2 = S2;
-    c.topk_idx = topk_idx; c.topk_w = topk_w; c.drop_mask = drop_mask;
-    c.tokens = tokens; c.y = y; c.slots = slots; c.shared_out = shared_out;
-    orc_parallel(ntok, orc_layer_range, &c);
+    oracle_layer_tokens_q(ntok, tokens, d, F, E, k, act, dtype, dtype, x, W1, W3, W2, b1, b2,
+                          NULL, NULL, NULL, F_sh, S1, S3, S2, topk_idx, topk_w, drop_mask, y,
+                          slots, shared_out);
 }
 
 /* ---------------------------------------------------------- step 10: aux */

@@ -37,11 +37,14 @@ class MoeConfig(ctypes.Structure):
                 ("E", ctypes.c_int), ("k", ctypes.c_int), ("F_shared", ctypes.c_int),
                 ("dtype", ctypes.c_int), ("act", ctypes.c_int), ("has_bias", ctypes.c_int),
                 ("capacity_factor", ctypes.c_float), ("scoring", ctypes.c_int),
-                ("no_renorm", ctypes.c_int)]
+                ("no_renorm", ctypes.c_int), ("weight_fp8", ctypes.c_int)]
+
+
+WEIGHT_KEYS = ("W1", "W3", "W2", "b1", "b2", "S1", "S3", "S2", "s1", "s3", "s2")
 
 
 class MoeWeights(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_void_p) for n in ("W1", "W3", "W2", "b1", "b2", "S1", "S3", "S2")]
+    _fields_ = [(n, ctypes.c_void_p) for n in WEIGHT_KEYS]
 
 
 class MoeLayerOut(ctypes.Structure):
@@ -100,7 +103,8 @@ def make_config(cfg: dict) -> MoeConfig:
         has_bias=int(bool(cfg.get("has_bias", False))),
         capacity_factor=float(cfg.get("capacity_factor", 0.0) or 0.0),
         scoring=MOE_SCORE_SIGMOID if cfg.get("scoring", "softmax") == "sigmoid" else MOE_SCORE_SOFTMAX,
-        no_renorm=0 if cfg.get("renorm", True) else 1)
+        no_renorm=0 if cfg.get("renorm", True) else 1,
+        weight_fp8=int(bool(cfg.get("weight_fp8", False))))
 
 
 def _p(t):
@@ -135,8 +139,7 @@ def new_workspace(cfg, device="cuda"):
 
 
 def _weights_struct(w: dict) -> MoeWeights:
-    return MoeWeights(*[None if w.get(n) is None else w[n].data_ptr()
-                        for n in ("W1", "W3", "W2", "b1", "b2", "S1", "S3", "S2")])
+    return MoeWeights(*[None if w.get(n) is None else w[n].data_ptr() for n in WEIGHT_KEYS])
 
 
 def route(cfg, x, Wr, logit_bias=None, ws=None, stream=None):

@@ -97,6 +97,11 @@ int check_cfg(const moe_cfg* c) {
     if (c->scoring != MOE_SCORE_SOFTMAX && c->scoring != MOE_SCORE_SIGMOID)
         return fail(MOE_ERR_INVALID_ARG, "unknown scoring%s");
     if (c->no_renorm != 0 && c->no_renorm != 1) return fail(MOE_ERR_INVALID_ARG, "no_renorm must be 0 or 1%s");
+    if (c->weight_fp8 != 0 && c->weight_fp8 != 1) return fail(MOE_ERR_INVALID_ARG, "weight_fp8 must be 0 or 1%s");
+    if (c->weight_fp8 && (c->dtype != MOE_BF16 || c->F_shared > 0))
+        return fail(MOE_ERR_UNSUPPORTED, "FP8 expert weights need a bf16 layer without a shared expert%s");
+    if (c->weight_fp8 && (c->d % 16 || c->F % 16))
+        return fail(MOE_ERR_INVALID_ARG, "FP8 expert weights need d and F multiples of 16 (16-byte rows)%s");
     return MOE_OK;
 }
 
@@ -145,6 +150,11 @@ int check_weights(const moe_cfg& c, const moe_weights* w) {
         MOE_TRY(check_ptr(w->S3, "S3"));
         MOE_TRY(check_ptr(w->S2, "S2"));
     }
+    if (c.weight_fp8) {
+        MOE_TRY(check_ptr4(w->s1, "s1"));
+        MOE_TRY(check_ptr4(w->s2, "s2"));
+        if (c.act == MOE_SWIGLU) MOE_TRY(check_ptr4(w->s3, "s3"));
+    }
     return MOE_OK;
 }
 
@@ -188,21 +198,25 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// bf16 row-major [rows, cols] matrix; box = box_rows rows x 64 columns (128
-// bytes), 128-byte swizzle, out-of-range elements read as zero.
+// Row-major [rows, cols] matrix of 2-byte elements (bf16, or f16 with
+// dt = CU_TENSOR_MAP_DATA_TYPE_FLOAT16); box = box_rows rows x 64 columns
+// (128 bytes), 128-byte swizzle, out-of-range elements read as zero.
+// 1-byte elements (E4M3 weights, dt = UINT8): 64-byte box rows, no swizzle.
 int encode_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, const char* what,
-                uint32_t box_rows = 128) {
+                uint32_t box_rows = 128,
+                CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
     auto fn = encode_fn();
     if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled unavailable%s");
     if (rows == 0) rows = 1;
+    const bool byte_elems = (dt == CU_TENSOR_MAP_DATA_TYPE_UINT8);
     const cuuint64_t dims[2] = {cols, rows};
-    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint64_t strides[1] = {cols * (byte_elems ? 1 : 2)};
     const cuuint32_t box[2] = {64, box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
-                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          byte_elems ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "tensor map encode failed for %s", what);
     return MOE_OK;
 }
@@ -294,6 +308,46 @@ int run_expert_ffn(const moe_cfg& c, const DevInfo& di, const void* x, const int
     void* H = at<char>(ws, L.h);
     void* Hsh = at<char>(ws, L.hsh);
     const int rows_sh = c.F_shared > 0 ? c.T : 0;
+    if (c.weight_fp8) {
+        if (di.cc != 103)
+            return fail(MOE_ERR_UNSUPPORTED, "FP8 expert GEMMs need an sm_103a (B300) device%s");
+        const int up_mode = c.act == MOE_SWIGLU ? kModeSwiglu : kModeGelu;
+        MOE_CUDA(launch_gather_f16(x, perm_src, offsets, c.E, c.k, c.T, c.d, Xp, status,
+                                   di.num_sms, st),
+                 "gather launch");
+        if (ev) MOE_CUDA(cudaEventRecord(ev[0], st), "event record");
+        CUtensorMap maps[3];
+        MOE_TRY(encode_rows(&maps[0], Xp, (uint64_t)A, c.d, "gathered rows", 128,
+                            CU_TENSOR_MAP_DATA_TYPE_FLOAT16));
+        MOE_TRY(encode_rows(&maps[1], w.W1, (uint64_t)c.E * c.F, c.d, "W1", 128,
+                            CU_TENSOR_MAP_DATA_TYPE_UINT8));
+        MOE_TRY(encode_rows(&maps[2], c.act == MOE_SWIGLU ? w.W3 : w.W1, (uint64_t)c.E * c.F, c.d,
+                            "W3", 128, CU_TENSOR_MAP_DATA_TYPE_UINT8));
+        TcFfnArgs up{};
+        up.offsets = offsets; up.E = c.E; up.N = c.F; up.K = c.d;
+        up.out = H;
+        up.bias = c.has_bias ? (const __nv_bfloat16*)w.b1 : nullptr;
+        up.status = status;
+        up.wscale = w.s1;
+        up.wscale2 = c.act == MOE_SWIGLU ? w.s3 : nullptr;
+        MOE_CUDA(launch_ffn_fp8(up_mode, maps, up, di.num_sms, st), "up-projection launch");
+        if (ev) MOE_CUDA(cudaEventRecord(ev[1], st), "event record");
+        MOE_TRY(encode_rows(&maps[0], H, (uint64_t)A, c.F, "hidden rows", 128,
+                            CU_TENSOR_MAP_DATA_TYPE_FLOAT16));
+        MOE_TRY(encode_rows(&maps[1], w.W2, (uint64_t)c.E * c.d, c.F, "W2", 128,
+                            CU_TENSOR_MAP_DATA_TYPE_UINT8));
+        maps[2] = maps[1];
+        TcFfnArgs dn{};
+        dn.offsets = offsets; dn.E = c.E; dn.N = c.d; dn.K = c.F;
+        dn.out = Ys;
+        dn.bias = c.has_bias ? (const __nv_bfloat16*)w.b2 : nullptr;
+        dn.perm_src = perm_src; dn.gate_w = topk_w;
+        dn.status = status;
+        dn.wscale = w.s2;
+        MOE_CUDA(launch_ffn_fp8(kModeDown, maps, dn, di.num_sms, st), "down-projection launch");
+        if (ev) MOE_CUDA(cudaEventRecord(ev[2], st), "event record");
+        return MOE_OK;
+    }
     MOE_CUDA(launch_gather(c.dtype, x, perm_src, offsets, c.E, c.k, c.T, c.d, Xp, status,
                            di.num_sms, st),
              "gather launch");

@@ -59,6 +59,9 @@ cudaError_t launch_dispatch(const int* topk_idx, int T, int k, int E, long long 
 cudaError_t launch_gather(int dtype, const void* x, const int* perm_src, const int* offsets, int E,
                           int k, int T, int d, void* Xp, int* status, int num_sms,
                           cudaStream_t st);
+// bf16 x -> f16 gathered rows (the FP8-weight path's token operand)
+cudaError_t launch_gather_f16(const void* x, const int* perm_src, const int* offsets, int E, int k,
+                              int T, int d, void* Xp, int* status, int num_sms, cudaStream_t st);
 cudaError_t launch_combine(int dtype, const void* x, const void* Ys, const unsigned char* drop_mask,
                            const void* Sh, void* y, int T, int d, int k, int num_sms,
                            cudaStream_t st);
@@ -95,11 +98,17 @@ struct TcFfnArgs {
     const int* perm_src;      // down
     const float* gate_w;      // down
     int* status;
+    const float* wscale;      // FP8 weights: per-row scales [E, N] (gate / fc1 / down)
+    const float* wscale2;     // FP8 SwiGLU: up-projection scales [E, N]
 };
 int ffn_tc_smem_bytes();
 // maps: A, B, B2, A_sh, B_sh, B2_sh (see ffn_tc.cu)
 cudaError_t launch_ffn_tc(int mode, const CUtensorMap* maps, const TcFfnArgs& p, int num_sms,
                           cudaStream_t st);
+// ffn_fp8.cu: FP8 (E4M3) weights with per-row scales; maps: A (f16 rows),
+// B (E4M3 rows, no swizzle), B2 (E4M3 up rows for SwiGLU)
+cudaError_t launch_ffn_fp8(int mode, const CUtensorMap* maps, const TcFfnArgs& p, int num_sms,
+                           cudaStream_t st);
 // ffn_tc2.cu: the same on CTA pairs (cta_group::2), 256-row tiles; same maps
 int ffn_tc2_tile_rows();
 cudaError_t launch_ffn_tc2(int mode, const CUtensorMap* maps, const TcFfnArgs& p, cudaStream_t st);

@@ -7,6 +7,8 @@
 // "How a sparse MoE layer works": the weighted sum is added through the
 // residual.  Both kernels move whole rows with 16-byte vectors; they are
 // bandwidth-bound and carry no arithmetic beyond the fp32 sum of the combine.
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "kernels.cuh"
 #include "launch.cuh"
@@ -34,6 +36,40 @@ gather_rows_kernel(const uint4* __restrict__ x, const int* __restrict__ perm_src
         const uint4* src = x + (size_t)t * vec_per_row;
         uint4* dst = Xp + (size_t)r * vec_per_row;
         for (int v = lane; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+    }
+}
+
+// As gather_rows_kernel, converting bf16 x to f16 on the way (the token
+// operand of the FP8-weight expert GEMMs, whose MMAs take f16).
+__global__ void __launch_bounds__(256)
+gather_rows_f16_kernel(const uint4* __restrict__ x, const int* __restrict__ perm_src,
+                       const int* __restrict__ offsets, int E, int k, int Ttok, int vec_per_row,
+                       uint4* __restrict__ Xp, int* __restrict__ status) {
+    pdl_wait();
+    pdl_trigger();
+    const int R = offsets[E];
+    const int warps = (gridDim.x * blockDim.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < R; r += warps) {
+        const int a = perm_src[r];
+        const int t = a / k;
+        if (a < 0 || t >= Ttok) {
+            if (lane == 0) raise_error(status, MOE_ERR_DEVICE_BOUNDS);
+            continue;
+        }
+        const uint4* src = x + (size_t)t * vec_per_row;
+        uint4* dst = Xp + (size_t)r * vec_per_row;
+        for (int v = lane; v < vec_per_row; v += 32) {
+            float f[8];
+            unpack16(__ldg(src + v), f);
+            uint32_t w[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const __half2 h = __floats2half2_rn(f[2 * j], f[2 * j + 1]);
+                w[j] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
     }
 }
 
@@ -88,6 +124,17 @@ cudaError_t launch_gather(int dtype, const void* x, const int* perm_src, const i
     if (blocks > num_sms * 16) blocks = num_sms * 16;
     if (blocks < 1) blocks = 1;
     return launch_kernel(gather_rows_kernel, dim3((unsigned)blocks), dim3(256), 0, st, 1,
+                         (const uint4*)x, perm_src, offsets, E, k, T, vpr, (uint4*)Xp, status);
+}
+
+cudaError_t launch_gather_f16(const void* x, const int* perm_src, const int* offsets, int E, int k,
+                              int T, int d, void* Xp, int* status, int num_sms, cudaStream_t st) {
+    const int vpr = d * 2 / 16;
+    const int A = T * k;
+    long long blocks = ((long long)A * 32 + 255) / 256;
+    if (blocks > num_sms * 16) blocks = num_sms * 16;
+    if (blocks < 1) blocks = 1;
+    return launch_kernel(gather_rows_f16_kernel, dim3((unsigned)blocks), dim3(256), 0, st, 1,
                          (const uint4*)x, perm_src, offsets, E, k, T, vpr, (uint4*)Xp, status);
 }
 

@@ -160,3 +160,47 @@ def to_device(inp: dict, device) -> dict:
     for key, v in inp.items():
         out[key] = v.to(device) if isinstance(v, torch.Tensor) else v
     return out
+
+
+FP8_MAX = 448.0     # largest finite E4M3 magnitude
+
+
+def quantize_experts_fp8(inp: dict) -> dict:
+    """Copy of a workload whose routed expert weights W1, W3, W2 are FP8 E4M3
+    codes with one fp32 scale per output row (s1, s3 [E,F], s2 [E,d]):
+    s = max|row| / 448 and code = E4M3(w / s), rounded to nearest-even by
+    torch's float8_e4m3fn conversion.  The dequantised weights are code * s.
+    Sets cfg['weight_fp8'].  Input preparation only, like drawing the weights."""
+    out = dict(inp)
+    cfg = dict(inp["cfg"])
+    cfg["weight_fp8"] = True
+    out["cfg"] = cfg
+    for key, skey in (("W1", "s1"), ("W3", "s3"), ("W2", "s2")):
+        w = inp.get(key)
+        if w is None:
+            out[key] = None
+            out[skey] = None
+            continue
+        codes = torch.empty(w.shape, dtype=torch.float8_e4m3fn, device=w.device)
+        scales = torch.empty(w.shape[:-1], dtype=torch.float32, device=w.device)
+        for e in range(w.shape[0]):          # one expert at a time bounds the fp32 temporary
+            wf = w[e].float()
+            sc = wf.abs().amax(dim=-1) / FP8_MAX
+            sc = torch.where(sc > 0, sc, torch.ones_like(sc))
+            scales[e] = sc
+            codes[e] = (wf / sc[:, None]).to(torch.float8_e4m3fn)
+        out[key] = codes
+        out[skey] = scales
+    return out
+
+
+def dequantize_experts_fp8(inp: dict) -> dict:
+    """fp32 copy of code * scale for each FP8 expert weight of `inp` (exact:
+    an E4M3 value times an fp32 scale is one fp32 rounding away at most, and
+    none at all when the product is representable; the oracle takes these
+    fp32 values as the weights)."""
+    out = dict(inp)
+    for key, skey in (("W1", "s1"), ("W3", "s3"), ("W2", "s2")):
+        if inp.get(key) is not None:
+            out[key] = inp[key].float() * inp[skey][..., None]
+    return out

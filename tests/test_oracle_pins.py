@@ -427,3 +427,40 @@ def test_aux_router_backward_products():
     np.testing.assert_allclose(gW, g.T @ x.astype(np.float64), rtol=1e-12, atol=1e-15)
     np.testing.assert_allclose(gx, g @ Wr.astype(np.float64), rtol=1e-12, atol=1e-15)
     assert gW.shape == (E, d) and gx.shape == (T, d)
+
+
+# ----------------------------------------------------- FP8 expert weights
+def test_e4m3_decoding_matches_torch_for_every_code():
+    """The oracle's E4M3 decoding (from the format's definition) equals
+    torch's float8_e4m3fn -> float64 conversion for all 256 codes (NaN codes
+    compared as NaN)."""
+    codes = torch.arange(256, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).double().numpy()
+    got = np.array([oracle.e4m3_value(c) for c in range(256)])
+    np.testing.assert_array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    np.testing.assert_array_equal(got[ok], ref[ok])
+    assert oracle.e4m3_value(0x7E) == 448.0 and oracle.e4m3_value(0x01) == 2.0 ** -9
+
+
+def test_fp8_expert_layer_equals_dequantised_fp64_layer():
+    """A layer with E4M3 expert weights and row scales equals the same layer
+    with the weights dequantised exactly (code * scale in double) by numpy."""
+    inp = workloads.make_inputs(workloads.config("mixtral_prefill", T=5, d=32, F=48, E=3, k=2,
+                                                 seed=41))
+    q = workloads.quantize_experts_fp8(inp)
+    tokens = np.arange(5)
+    routed = oracle.layer_forward(q, tokens=tokens)
+    xf = inp["x"].double().numpy()
+    for r, t in enumerate(tokens):
+        ref = xf[t].copy()
+        for s in range(2):
+            e = routed["topk_idx"][t, s]
+            W1 = q["W1"][e].view(torch.uint8).numpy()
+            deq = lambda key, skey: (np.vectorize(oracle.e4m3_value)(q[key][e].view(torch.uint8).numpy())
+                                     * q[skey][e].double().numpy()[:, None])
+            g = deq("W1", "s1") @ xf[t]
+            u = deq("W3", "s3") @ xf[t]
+            h = g * expit(g) * u
+            ref += routed["topk_w"][t, s] * (deq("W2", "s2") @ h)
+        np.testing.assert_allclose(routed["y"][r], ref, rtol=1e-12, atol=1e-12)
