@@ -39,10 +39,15 @@ int router_blocks(int T) {
 }
 
 struct Layout {
-    size_t ctrl, tile_status, rank, prob_part, prob_mean, router_part, logits, topk_idx, topk_w,
+    size_t ctrl, tile_status, split_ticket, rank, prob_part, prob_mean, router_part, logits, topk_idx, topk_w,
         counts_pre, counts_kept, offsets, perm_src, dest, drop_mask, stats, xp, h, hsh, ys, sh,
-        total;
+        split_part, total;
 };
+
+// FP8 expert GEMMs: tickets and fp32 partial sums of the tiles that straddle
+// two CTAs' stream-K ranges (ffn_fp8.cu).
+constexpr int kFp8SplitTickets = kFp8MaxGrid;
+size_t fp8_split_bytes(const moe_cfg&) { return kFp8SplitBytes; }
 
 Layout layout_of(const moe_cfg& c) {
     Layout L;
@@ -51,6 +56,7 @@ Layout layout_of(const moe_cfg& c) {
     auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes); return at; };
     L.ctrl = take(kCtrlWords * 4);
     L.tile_status = take((size_t)dispatch_blocks((int)A) * E * 4);
+    L.split_ticket = take(c.weight_fp8 ? (size_t)kFp8SplitTickets * 4 : 0);
     L.rank = take(A * 4);
     L.prob_part = take((size_t)router_blocks(c.T) * E * 4);
     L.prob_mean = take(E * 4);
@@ -72,6 +78,7 @@ Layout layout_of(const moe_cfg& c) {
     L.hsh = take(T * (size_t)c.F_shared * es);
     L.ys = take(A * c.d * es);
     L.sh = take(c.F_shared > 0 ? T * c.d * es : 0);
+    L.split_part = take(c.weight_fp8 ? fp8_split_bytes(c) : 0);
     L.total = o;
     return L;
 }
@@ -204,18 +211,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // 1-byte elements (E4M3 weights, dt = UINT8): 64-byte box rows, no swizzle.
 int encode_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, const char* what,
                 uint32_t box_rows = 128,
-                CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
+                CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                uint32_t box_cols = 64) {
     auto fn = encode_fn();
     if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled unavailable%s");
     if (rows == 0) rows = 1;
     const bool byte_elems = (dt == CU_TENSOR_MAP_DATA_TYPE_UINT8);
     const cuuint64_t dims[2] = {cols, rows};
     const cuuint64_t strides[1] = {cols * (byte_elems ? 1 : 2)};
-    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          byte_elems ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "tensor map encode failed for %s", what);
     return MOE_OK;
@@ -317,13 +324,18 @@ int run_expert_ffn(const moe_cfg& c, const DevInfo& di, const void* x, const int
                  "gather launch");
         if (ev) MOE_CUDA(cudaEventRecord(ev[0], st), "event record");
         CUtensorMap maps[3];
-        MOE_TRY(encode_rows(&maps[0], Xp, (uint64_t)A, c.d, "gathered rows", 128,
+        MOE_TRY(encode_rows(&maps[0], Xp, (uint64_t)A, c.d, "gathered rows", 16,
                             CU_TENSOR_MAP_DATA_TYPE_FLOAT16));
-        MOE_TRY(encode_rows(&maps[1], w.W1, (uint64_t)c.E * c.F, c.d, "W1", 128,
-                            CU_TENSOR_MAP_DATA_TYPE_UINT8));
+        MOE_TRY(encode_rows(&maps[1], w.W1, (uint64_t)c.E * c.F, c.d, "W1", 64,
+                            CU_TENSOR_MAP_DATA_TYPE_UINT8, 128));
         MOE_TRY(encode_rows(&maps[2], c.act == MOE_SWIGLU ? w.W3 : w.W1, (uint64_t)c.E * c.F, c.d,
-                            "W3", 128, CU_TENSOR_MAP_DATA_TYPE_UINT8));
+                            "W3", 64, CU_TENSOR_MAP_DATA_TYPE_UINT8, 128));
+        int* tickets = at<int>(ws, L.split_ticket);
+        float* part = at<float>(ws, L.split_part);
+        const long long part_bytes = (long long)fp8_split_bytes(c);
         TcFfnArgs up{};
+        up.split_ticket = tickets; up.split_tickets = kFp8SplitTickets;
+        up.split_part = part; up.split_bytes = part_bytes;
         up.offsets = offsets; up.E = c.E; up.N = c.F; up.K = c.d;
         up.out = H;
         up.bias = c.has_bias ? (const __nv_bfloat16*)w.b1 : nullptr;
@@ -332,12 +344,14 @@ int run_expert_ffn(const moe_cfg& c, const DevInfo& di, const void* x, const int
         up.wscale2 = c.act == MOE_SWIGLU ? w.s3 : nullptr;
         MOE_CUDA(launch_ffn_fp8(up_mode, maps, up, di.num_sms, st), "up-projection launch");
         if (ev) MOE_CUDA(cudaEventRecord(ev[1], st), "event record");
-        MOE_TRY(encode_rows(&maps[0], H, (uint64_t)A, c.F, "hidden rows", 128,
+        MOE_TRY(encode_rows(&maps[0], H, (uint64_t)A, c.F, "hidden rows", 16,
                             CU_TENSOR_MAP_DATA_TYPE_FLOAT16));
-        MOE_TRY(encode_rows(&maps[1], w.W2, (uint64_t)c.E * c.d, c.F, "W2", 128,
-                            CU_TENSOR_MAP_DATA_TYPE_UINT8));
+        MOE_TRY(encode_rows(&maps[1], w.W2, (uint64_t)c.E * c.d, c.F, "W2", 64,
+                            CU_TENSOR_MAP_DATA_TYPE_UINT8, 128));
         maps[2] = maps[1];
         TcFfnArgs dn{};
+        dn.split_ticket = tickets; dn.split_tickets = kFp8SplitTickets;
+        dn.split_part = part; dn.split_bytes = part_bytes;
         dn.offsets = offsets; dn.E = c.E; dn.N = c.d; dn.K = c.F;
         dn.out = Ys;
         dn.bias = c.has_bias ? (const __nv_bfloat16*)w.b2 : nullptr;

@@ -8,20 +8,63 @@
 //   SwiGLU  H = silu(s1 (A q1^T)) * (s3 (A q3^T))
 //   GELU    H = gelu(s1 (A q1^T) + b1)
 //   down    Ys[perm_src[r]] = topk_w * (s2 (H q2^T) + b2)
-// Tokens on M (128-row tiles), one CTA per SM, 320 threads:
-//   warp 0      TMA: f16 token tile 128x64 and the FP8 weight tile 256x64
-//               (no swizzle, 64-byte rows) into a 4-stage ring;
-//   warps 6-9   converters: E4M3 -> f16 (exact) straight into the 128-byte
-//               swizzled operand layout of one of two f16 weight buffers,
-//               then a proxy fence so the tensor core sees the writes;
-//   warp 1      TMEM + tcgen05.mma kind::f16 (M=128, N=256, K=16);
-//   warps 2-5   epilogue: scale the fp32 accumulator by the row scales, fused
-//               activation / gate scale, f16 H (A operand of the down GEMM)
-//               or bf16 slot outputs.
+//
+// Decode batches give each expert a handful of tokens, so the weights are the
+// MMA's M operand and the tokens its N operand (at most 32 per tile, rounded
+// up to 16).  A weight block is 128 rows: 64 gate + 64 up rows of the same
+// hidden units for SwiGLU, else 128 consecutive outputs.  A tile is G = 4
+// weight blocks of one expert against one token tile, so that each k-block of
+// tokens is loaded once for 4 blocks.  (While the weight stream saturates HBM
+// every load of an SM waits several microseconds -- its in-flight bytes over
+// its share of the bandwidth -- L2 hits included; token loads of 4 KB per 16 KB
+// weight stage would both slow the weight stream and arrive late for the
+// MMAs.)
+//
+// The converted f16 weights go to tensor memory, which the MMA reads as its A
+// operand: staging them in shared memory instead would move about 6.5
+// shared-memory bytes per weight byte (TMA write, converter read and write,
+// MMA read), which at 128 B/clock caps the weight stream near the HBM rate;
+// through TMEM it is 2 bytes.
+//
+// One CTA per SM, 576 threads:
+//   warp 0      TMA: E4M3 weight rows (128 bytes of K, 128-byte swizzle) into
+//               a 9-stage ring that the converters release as soon as they
+//               hold a stage's codes in registers;
+//   warp 14     TMA: the tile's f16 token rows (128-byte swizzle) in chunks of
+//               up to 24 KB into two buffers, a chunk ahead;
+//   warps 6-13  converters, one thread per weight row and half of the stage's
+//               K: E4M3 -> f16 pairs in registers, tcgen05.st into the TMEM A
+//               buffer of the stage's block;
+//   warps 1, 15-17  MMA issuers, issuer i for block i of the tile:
+//               tcgen05.mma kind::f16 (M=128, N=tokens, K=16), A from its TMEM
+//               buffer, B (tokens) from shared memory, into the block's
+//               accumulator.  A thread issues a small MMA only every ~50-100
+//               clocks, and a stage needs 8, so one issuer could not keep up
+//               with the weight stream; warp 1 also owns the TMEM allocation;
+//   warps 2-5   epilogue: row scales, fused activation / gate scale, f16 H
+//               (A operand of the down GEMM) or bf16 slot outputs.  The
+//               scales, biases and token slots of a tile are copied to shared
+//               memory before its accumulators are ready: a global load waits
+//               several microseconds while the weight stream runs.
+//
+// The conversion is integer work, no float arithmetic: an E4M3 code with sign
+// s, exponent field e (bias 7) and mantissa m is, re-laid as an f16 bit
+// pattern (sign at bit 15, e at bits 13..10, m at bits 9..7), the f16 number
+// code * 2^-8 (f16 bias 15 = 7 + 8; E4M3 subnormals become f16 subnormals
+// with the same mantissa).  The 2^8 goes into the row scale, exactly.
+//
+// Work balance (stream-K): the W = tiles x k-blocks units of work are cut into
+// one contiguous range per CTA.  A tile that lies in one range is finished
+// from TMEM; a tile that straddles ranges is accumulated in parts, each part
+// writes fp32 partial sums to its CTA's slot, and the CTA that finishes the
+// tile's last part (a ticket counter) adds the parts in CTA order and runs the
+// epilogue -- deterministic whatever the finishing order.  A CTA takes its
+// shared tiles first (the one its range starts inside, the one it ends inside)
+// and its whole tiles after, so that the partial sums and their reductions
+// overlap the work that follows instead of trailing it.
 #include <cuda_fp16.h>
 
 #include "common.cuh"
-#include "ffn_tc_common.cuh"
 #include "kernels.cuh"
 #include "launch.cuh"
 #include "tc_ptx.cuh"
@@ -30,169 +73,240 @@ namespace moe {
 
 namespace {
 
-using tcffn::BK;
-using tcffn::ModeTraits;
-using tcffn::Tile;
-
-constexpr int BM = 128;
-constexpr int MMA_N = 256;
-constexpr int STAGES = 4;
-constexpr int NB16 = 2;
-constexpr int A_BYTES = BM * BK * 2;          // f16 tokens
-constexpr int BQ_BYTES = MMA_N * BK;           // FP8 weights, 64-byte rows
-constexpr int B16_BYTES = MMA_N * BK * 2;      // converted f16 weights, swizzled
+constexpr int BK = 128;                        // K per stage: one 128-byte row of codes
+constexpr int WROWS = 128;                     // weight rows per block (MMA M, TMEM lanes)
+constexpr int G = 4;                           // weight blocks per tile
+constexpr int NISS = G;                        // MMA issuers and TMEM A buffers, one per block
+constexpr int TOK = 32;                        // tokens per tile at most (MMA N)
+constexpr int TOK_BOX = 16;                    // token rows per TMA box
+constexpr int WSTAGES = 9;                     // E4M3 weight ring
+constexpr int TB_BYTES = 24 * 1024;            // token chunk buffer (two of them)
+constexpr int WQ_BYTES = WROWS * BK;           // E4M3 codes of one stage
+constexpr int A_COLS = BK / 2;                 // TMEM columns of one A buffer (f16 pairs)
+constexpr int ACC_SET = G * TOK;               // TMEM columns of a tile's accumulators
+constexpr int A_COL0 = 2 * ACC_SET;            // two accumulator sets, then the A buffers
 constexpr int TMEM_COLS = 512;
-constexpr int NUM_THREADS = 320;
-constexpr int CVT_THREADS = 128;
-constexpr uint32_t IDESC = ptx::idesc_f16_f32(BM, MMA_N);
+static_assert(A_COL0 + NISS * A_COLS <= TMEM_COLS, "tensor memory budget");
+constexpr int CVT_WARPS = 8;
+constexpr int TOKP_WARP = 6 + CVT_WARPS;      // token producer
+constexpr int MMA_WARP1 = TOKP_WARP + 1;      // issuers 1..NISS-1 (issuer 0: warp 1)
+constexpr int NUM_THREADS = (MMA_WARP1 + NISS - 1) * 32;
+constexpr int XCH_LD = 33;
 
-constexpr int OFF_A = 0;
-constexpr int OFF_BQ = STAGES * A_BYTES;
-constexpr int OFF_B16 = OFF_BQ + STAGES * BQ_BYTES;
-constexpr int OFF_BAR = OFF_B16 + NB16 * B16_BYTES;
-constexpr int NUM_BARS = 2 * STAGES + 2 * NB16 + 2 + 2 + 1;
+constexpr int OFF_TOK = 0;
+constexpr int OFF_WQ = OFF_TOK + 2 * TB_BYTES;
+constexpr int OFF_XCH = OFF_WQ + WSTAGES * WQ_BYTES;
+constexpr int OFF_PRE = OFF_XCH + 64 * XCH_LD * 4;   // [2][G][128] row scales, biases
+constexpr int OFF_TOKA = OFF_PRE + 2 * G * WROWS * 4;
+constexpr int OFF_TOKW = OFF_TOKA + 2 * TOK * 4;     // token slots and weights, 2 buffers
+constexpr int OFF_BAR = OFF_TOKW + 2 * TOK * 4;
+constexpr int NUM_BARS = 2 * WSTAGES + 2 + 2 + 2 * NISS + 2 + 2 + NISS;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-constexpr int OFF_START = OFF_MISC + 16;
+constexpr int OFF_START = OFF_MISC + 32;
 constexpr int OFF_OFFS = OFF_START + (kMaxExperts + 2) * 4;
 constexpr int SMEM_USED = OFF_OFFS + (kMaxExperts + 2) * 4;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;
-static_assert(OFF_B16 % 1024 == 0, "swizzled f16 operand buffers need 1024-byte alignment");
+static_assert(OFF_TOK % 1024 == 0 && TB_BYTES % 1024 == 0, "swizzled token atoms");
+static_assert(OFF_WQ % 1024 == 0 && WQ_BYTES % 1024 == 0, "swizzled weight stages");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
-__device__ __forceinline__ void store_row32_f16(__half* dst, const float (&v)[32], int ncols) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        if (q * 8 < ncols) {
-            uint32_t w[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const __half2 h = __floats2half2_rn(v[q * 8 + 2 * j], v[q * 8 + 2 * j + 1]);
-                w[j] = *reinterpret_cast<const uint32_t*>(&h);
+template <int MODE>
+struct Fp8Traits {
+    // output units (hidden units for SwiGLU, output columns otherwise) per block
+    static constexpr int UNITS = MODE == kModeSwiglu ? 64 : 128;
+};
+
+// Four E4M3 codes (byte i = code i) -> four f16 equal to code * 2^-8, in two
+// words (codes 0,1 in lo; 2,3 in hi; lower code in the lower half).
+// High byte of each f16: sign | e << 2 | m >> 1; low byte: (m & 1) << 7.
+__device__ __forceinline__ void e4m3x4_to_f16x4_pow2(uint32_t x, uint32_t& lo, uint32_t& hi) {
+    const uint32_t hb = (x & 0x80808080u) | ((x & 0x7e7e7e7eu) >> 1);
+    const uint32_t lb = (x & 0x01010101u) << 7;
+    lo = __byte_perm(lb, hb, 0x5140);
+    hi = __byte_perm(lb, hb, 0x7362);
+}
+
+// Stream-K ranges: CTA c owns work units [cta_start(c), cta_start(c + 1)).
+__device__ __forceinline__ long long cta_start(long long W, int grid, int c) {
+    return (long long)c * W / grid;
+}
+// The CTA that owns unit x: the largest c with cta_start(c) <= x.
+__device__ __forceinline__ int cta_of(long long x, long long W, int grid) {
+    return (int)(((x + 1) * grid + W - 1) / W) - 1;
+}
+
+// One CTA's part of one tile: k-blocks [kb0, kb1).
+struct Seg {
+    int tile;
+    int g;             // expert
+    int tok0, ntok;    // first gathered row, valid tokens
+    int nmma;          // MMA N: ntok rounded up to 16
+    int blk0, nblk;    // first weight block (within the expert), blocks in the tile
+    int kb0, kb1;
+    int c_first, c_last;  // CTAs whose ranges meet the tile
+};
+
+// Tiles enumerate (expert, block group, token tile), token tile fastest.
+__device__ __forceinline__ Seg decode_seg(const TcFfnArgs& p, const int* s_start, const int* s_off,
+                                          int nwb, int nk, long long W, int tile, int kb0,
+                                          int kb1) {
+    Seg t;
+    t.tile = tile;
+    t.g = find_group(s_start, p.E, tile);
+    const int seg0 = s_off[t.g];
+    const int rows = s_off[t.g + 1] - seg0;
+    const int ntt = (rows + TOK - 1) / TOK;
+    const int local = tile - s_start[t.g];
+    const int wbg = local / ntt, tt = local - wbg * ntt;
+    t.tok0 = seg0 + tt * TOK;
+    t.ntok = min(TOK, rows - tt * TOK);
+    t.nmma = (t.ntok + 15) & ~15;
+    t.blk0 = wbg * G;
+    t.nblk = min(G, nwb - t.blk0);
+    t.kb0 = kb0;
+    t.kb1 = kb1;
+    const int grid = (int)gridDim.x;
+    t.c_first = cta_of((long long)tile * nk, W, grid);
+    t.c_last = cta_of((long long)tile * nk + nk - 1, W, grid);
+    return t;
+}
+
+// Weight rows of block j of a tile: the first rows of its two 64-row boxes.
+template <int MODE>
+__device__ __forceinline__ int2 block_rows(const TcFfnArgs& p, const Seg& t, int j) {
+    const int u0 = (t.blk0 + j) * Fp8Traits<MODE>::UNITS;
+    const int r0 = t.g * p.N + u0;
+    return make_int2(r0, MODE == kModeSwiglu ? r0 : r0 + 64);
+}
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Epilogue of one block's accumulator (tokens 0..31) for the calling thread's
+// weight row `row`; v holds the raw sums (weights at 2^-8 scale).
+// Row scales (times 2^8) and biases of the tile's blocks for the calling
+// thread's weight row, into its own slots of the prefetch area.
+template <int MODE>
+__device__ __forceinline__ void prefetch_rows(const TcFfnArgs& p, const Seg& t, int row,
+                                              float* s_pre) {
+    const size_t sbase = (size_t)t.g * p.N;
+    for (int j = 0; j < t.nblk; ++j) {
+        const int u0 = (t.blk0 + j) * Fp8Traits<MODE>::UNITS;
+        float sc = 0.f, b = 0.f;
+        if (MODE == kModeSwiglu) {
+            const int u = u0 + (row & 63);
+            if (u < p.N) sc = 256.f * (row < 64 ? p.wscale : p.wscale2)[sbase + u];
+        } else {
+            const int n = u0 + row;
+            if (n < p.N) {
+                sc = 256.f * p.wscale[sbase + n];
+                if (p.bias) b = __bfloat162float(p.bias[sbase + n]);
             }
-            reinterpret_cast<uint4*>(dst)[q] = make_uint4(w[0], w[1], w[2], w[3]);
         }
+        s_pre[j * WROWS + row] = sc;
+        s_pre[G * WROWS + j * WROWS + row] = b;
     }
 }
 
-// Epilogue of one accumulator for the thread's row r (a global A row).
 template <int MODE>
-__device__ __forceinline__ void epilogue_fp8(const TcFfnArgs& p, const Tile& t, uint32_t taddr,
-                                             int r) {
-    constexpr int BN_OUT = ModeTraits<MODE>::BN_OUT;
-    const bool row_ok = r < t.row_end;
-    const size_t srow = (size_t)t.g * t.N;          // this group's first scale
+__device__ __forceinline__ void finish_block(const TcFfnArgs& p, const Seg& t, int j, int row,
+                                             float (&v)[32], float* s_xch, const float* s_pre,
+                                             const int* s_tok_a, const float* s_tok_w) {
+    const int u0 = (t.blk0 + j) * Fp8Traits<MODE>::UNITS;
+    const float sc = s_pre[j * WROWS + row];
     if (MODE == kModeSwiglu) {
-        __half* dst = reinterpret_cast<__half*>(p.out) + (size_t)r * t.N + t.n0;
-#pragma unroll 1
-        for (int c = 0; c < BN_OUT; c += 32) {
-            __syncwarp();
-            float g[32], u[32];
-            ptx::tmem_ld32(taddr + c, g);
-            ptx::tmem_ld32(taddr + 128 + c, u);
-            const int ncols = t.N - (t.n0 + c);
-            if (row_ok && ncols > 0) {
+        const int u = u0 + (row & 63);
+        const bool u_ok = u < p.N;
+        if (row >= 64) {
+            float* xr = s_xch + (row - 64) * XCH_LD;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int n = t.n0 + c + j;
-                    const float sg = n < t.N ? p.wscale[srow + n] : 0.f;
-                    const float su = n < t.N ? p.wscale2[srow + n] : 0.f;
-                    g[j] = silu(g[j] * sg) * (u[j] * su);
-                }
-                store_row32_f16(dst + c, g, ncols);
-            }
+            for (int c = 0; c < 32; ++c) xr[c] = v[c] * sc;
         }
-    } else if (MODE == kModeGelu) {
-        __half* dst = reinterpret_cast<__half*>(p.out) + (size_t)r * t.N + t.n0;
-        const __nv_bfloat16* bias = p.bias ? p.bias + srow : nullptr;
-#pragma unroll 1
-        for (int c = 0; c < BN_OUT; c += 32) {
-            __syncwarp();
-            float v[32];
-            ptx::tmem_ld32(taddr + c, v);
-            const int ncols = t.N - (t.n0 + c);
-            if (row_ok && ncols > 0) {
+        epi_bar();
+        if (row < 64 && u_ok) {
+            const float sg = sc;
+            const float* xr = s_xch + row * XCH_LD;
+            __half* H = reinterpret_cast<__half*>(p.out);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int n = t.n0 + c + j;
-                    const float sc = n < t.N ? p.wscale[srow + n] : 0.f;
-                    const float b = (bias && n < t.N) ? __bfloat162float(bias[n]) : 0.f;
-                    v[j] = gelu_erf(v[j] * sc + b);
-                }
-                store_row32_f16(dst + c, v, ncols);
-            }
+            for (int c = 0; c < 32; ++c)
+                if (c < t.ntok)
+                    H[(size_t)(t.tok0 + c) * p.N + u] = __float2half_rn(silu(v[c] * sg) * xr[c]);
         }
+        epi_bar();
     } else {
-        __nv_bfloat16* dst = nullptr;
-        float gate = 1.f;
-        if (row_ok) {
-            const int a = p.perm_src[r];
-            gate = p.gate_w[a];
-            dst = reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t)a * t.N + t.n0;
-        }
-        const __nv_bfloat16* bias = p.bias ? p.bias + srow : nullptr;
-#pragma unroll 1
-        for (int c = 0; c < BN_OUT; c += 32) {
-            __syncwarp();
-            float v[32];
-            ptx::tmem_ld32(taddr + c, v);
-            const int ncols = t.N - (t.n0 + c);
-            if (row_ok && ncols > 0) {
+        const int n = u0 + row;
+        if (n >= p.N) return;
+        const float b = s_pre[G * WROWS + j * WROWS + row];
+        if (MODE == kModeGelu) {
+            __half* H = reinterpret_cast<__half*>(p.out);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int n = t.n0 + c + j;
-                    const float sc = n < t.N ? p.wscale[srow + n] : 0.f;
-                    const float b = (bias && n < t.N) ? __bfloat162float(bias[n]) : 0.f;
-                    v[j] = gate * (v[j] * sc + b);
-                }
-                tcffn::store_row32(dst + c, v, ncols);
-            }
+            for (int c = 0; c < 32; ++c)
+                if (c < t.ntok)
+                    H[(size_t)(t.tok0 + c) * p.N + n] = __float2half_rn(gelu_erf(v[c] * sc + b));
+        } else {
+            __nv_bfloat16* Ys = reinterpret_cast<__nv_bfloat16*>(p.out);
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+                if (c < t.ntok)
+                    Ys[(size_t)s_tok_a[c] * p.N + n] = __float2bfloat16_rn(s_tok_w[c] * (v[c] * sc + b));
         }
     }
 }
 
 template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
-               const __grid_constant__ CUtensorMap mapB2, const TcFfnArgs p) {
+ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__ CUtensorMap mapW,
+               const __grid_constant__ CUtensorMap mapW3, const TcFfnArgs p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t* sA = smem + OFF_A;
-    uint8_t* sBq = smem + OFF_BQ;
-    uint8_t* sB16 = smem + OFF_B16;
+    uint8_t* sTok = smem + OFF_TOK;
+    uint8_t* sWq = smem + OFF_WQ;
+    float* s_xch = reinterpret_cast<float*>(smem + OFF_XCH);
+    float* s_pre = reinterpret_cast<float*>(smem + OFF_PRE);
+    int* s_tok_a = reinterpret_cast<int*>(smem + OFF_TOKA);
+    float* s_tok_w = reinterpret_cast<float*>(smem + OFF_TOKW);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-    uint64_t* full = bars;                       // TMA landed (tokens + FP8 weights)
-    uint64_t* empty = full + STAGES;             // MMA done with the stage
-    uint64_t* cfull = empty + STAGES;            // converted f16 weights ready
-    uint64_t* cempty = cfull + NB16;             // MMA done with the f16 buffer
-    uint64_t* tfull = cempty + NB16;
+    uint64_t* wfull = bars;                      // E4M3 codes landed
+    uint64_t* wempty = wfull + WSTAGES;          // converters hold the codes
+    uint64_t* kfull = wempty + WSTAGES;          // a token chunk landed
+    uint64_t* kempty = kfull + 2;                // the issuers done with the chunk
+    uint64_t* cfull = kempty + 2;                // converted weights in issuer i's A buffer
+    uint64_t* cempty = cfull + NISS;             // issuer i's MMAs done with it
+    uint64_t* tfull = cempty + NISS;             // the issuers' accumulators complete
     uint64_t* tempty = tfull + 2;
-    uint64_t* drain = tempty + 2;
+    uint64_t* drain = tempty + 2;                // per issuer
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
     volatile int* s_abort = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+    volatile int* s_go = reinterpret_cast<volatile int*>(smem + OFF_MISC + 8);
+    volatile int* s_last = reinterpret_cast<volatile int*>(smem + OFF_MISC + 12);
+    int* s_maxrows = reinterpret_cast<int*>(smem + OFF_MISC + 16);
     int* s_start = reinterpret_cast<int*>(smem + OFF_START);
     int* s_off = reinterpret_cast<int*>(smem + OFF_OFFS);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            ptx::mbar_init(&full[s], 1);
-            ptx::mbar_init(&empty[s], 1);
+        for (int s = 0; s < WSTAGES; ++s) {
+            ptx::mbar_init(&wfull[s], 1);
+            ptx::mbar_init(&wempty[s], CVT_WARPS);
         }
-        for (int b = 0; b < NB16; ++b) {
-            ptx::mbar_init(&cfull[b], CVT_THREADS);
+        for (int s = 0; s < 2; ++s) {
+            ptx::mbar_init(&kfull[s], 1);
+            ptx::mbar_init(&kempty[s], NISS);
+        }
+        for (int b = 0; b < NISS; ++b) {
+            ptx::mbar_init(&cfull[b], CVT_WARPS);
             ptx::mbar_init(&cempty[b], 1);
         }
         for (int a = 0; a < 2; ++a) {
-            ptx::mbar_init(&tfull[a], 1);
+            ptx::mbar_init(&tfull[a], NISS);
             ptx::mbar_init(&tempty[a], 128);
         }
-        ptx::mbar_init(drain, 1);
+        for (int j = 0; j < NISS; ++j) ptx::mbar_init(&drain[j], 1);
         *s_abort = 0;
         ptx::fence_mbarrier_init();
-        ptx::prefetch_tensormap(&mapA);
-        ptx::prefetch_tensormap(&mapB);
-        ptx::prefetch_tensormap(&mapB2);
+        ptx::prefetch_tensormap(&mapX);
+        ptx::prefetch_tensormap(&mapW);
+        ptx::prefetch_tensormap(&mapW3);
     }
     if (warp == 1) {
         ptx::tmem_alloc(s_tmem, TMEM_COLS);
@@ -201,147 +315,350 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
     pdl_wait();
     pdl_trigger();
     for (int i = threadIdx.x; i <= p.E; i += NUM_THREADS) s_off[i] = p.offsets[i];
-    constexpr int BN_OUT = ModeTraits<MODE>::BN_OUT;
-    const int nt_r = (p.N + BN_OUT - 1) / BN_OUT;
-    group_tile_prefix(p.offsets, p.E, 0, BM, nt_r, 0, s_start);
+    const int nwb = (p.N + Fp8Traits<MODE>::UNITS - 1) / Fp8Traits<MODE>::UNITS;
+    if (warp == 0) {            // longest segment: sizes the token chunks
+        int m = 0;
+        for (int g = lane; g < p.E; g += 32) m = max(m, p.offsets[g + 1] - p.offsets[g]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) *s_maxrows = m;
+    }
+    group_tile_prefix(p.offsets, p.E, 0, TOK, (nwb + G - 1) / G, 0, s_start);
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *s_tmem;
-    const int G = p.E;
-    const int total = s_start[G];
+    const int grid = (int)gridDim.x;
+    const int nk = (p.K + BK - 1) / BK;
+    const long long W = (long long)s_start[p.E] * nk;
+    const long long my0 = cta_start(W, grid, blockIdx.x);
+    const long long my1 = cta_start(W, grid, blockIdx.x + 1);
+    const long long slot_floats = (long long)WROWS * TOK;              // one block's partials
+    // k-blocks per token chunk: the widest token tile fills a buffer
+    const int CH = TB_BYTES / (min(TOK, max(16, (*s_maxrows + 15) & ~15)) * 256);
+    // room for two slots of G blocks per CTA and a ticket per CTA
+    const bool room = p.split_ticket && grid <= p.split_tickets &&
+                      2LL * grid * G * slot_floats * 4 <= p.split_bytes;
+    long long end = my1;
+    if (!room && W > 0) {
+        if (threadIdx.x == 0) raise_error(p.status, MOE_ERR_INVALID_ARG);
+        end = my0;                                                    // no work
+    }
+    // The segments of this CTA; every role walks the same list: the shared
+    // head tile (the range starts inside it), the shared tail tile (the range
+    // ends inside it), then the whole tiles in order.
+    const int t_first = (int)(my0 / nk);
+    const int t_last = end > my0 ? (int)((end - 1) / nk) : t_first - 1;
+    const int head_kb0 = (int)(my0 - (long long)t_first * nk);
+    const int tail_kb1 = (int)(end - (long long)t_last * nk);
+    const bool single = t_first == t_last;
+    const int head_part = !single && head_kb0 > 0;
+    const int tail_part = !single && tail_kb1 < nk;
+    const int nseg = t_last < t_first ? 0 : single ? 1 : t_last - t_first + 1;
+    auto seg_of = [&](int i, int& tile, int& kb0, int& kb1) {
+        if (single) { tile = t_first; kb0 = head_kb0; kb1 = tail_kb1; return; }
+        if (head_part) {
+            if (i == 0) { tile = t_first; kb0 = head_kb0; kb1 = nk; return; }
+            --i;
+        }
+        if (tail_part) {
+            if (i == 0) { tile = t_last; kb0 = 0; kb1 = tail_kb1; return; }
+            --i;
+        }
+        tile = t_first + head_part + i;
+        kb0 = 0;
+        kb1 = nk;
+    };
+#define FOR_EACH_SEG(t)                                                                    \
+    for (int si_ = 0; si_ < nseg; ++si_) {                                                 \
+        int tile_, kb0_, kb1_;                                                             \
+        seg_of(si_, tile_, kb0_, kb1_);                                                    \
+        const Seg t = decode_seg(p, s_start, s_off, nwb, nk, W, tile_, kb0_, kb1_);
 
     if (warp == 0) {
-        // ------------------------------------------------------ TMA producer
+        // ------------------------------------------------ TMA producer (weights)
         if (lane == 0) {
             int it = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-                const Tile t = tcffn::decode_tile<MODE, BM>(p, s_start, s_off, G, tile);
-                const CUtensorMap* mB1 = (MODE == kModeSwiglu) ? &mapB2 : &mapB;
-                for (int kb = 0; kb < t.nk; ++kb, ++it) {
-                    const int s = it % STAGES;
-                    const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
-                    if (!ptx::mbar_wait(&empty[s], ph ^ 1u, s_abort)) { ok = false; break; }
-                    ptx::mbar_arrive_expect_tx(&full[s], A_BYTES + BQ_BYTES);
-                    ptx::tma_load_2d(sA + s * A_BYTES, &mapA, &full[s], kb * BK, t.arow);
-                    ptx::tma_load_2d(sBq + s * BQ_BYTES, &mapB, &full[s], kb * BK, t.wrow0);
-                    ptx::tma_load_2d(sBq + s * BQ_BYTES + BQ_BYTES / 2, mB1, &full[s], kb * BK,
-                                     t.wrow1);
-                }
+            FOR_EACH_SEG(t)
+                for (int kb = t.kb0; ok && kb < t.kb1; ++kb)
+                    for (int j = 0; j < t.nblk; ++j, ++it) {
+                        const int s = it % WSTAGES;
+                        const uint32_t ph = (uint32_t)(it / WSTAGES) & 1u;
+                        if (!ptx::mbar_wait(&wempty[s], ph ^ 1u, s_abort)) { ok = false; break; }
+                        ptx::mbar_arrive_expect_tx(&wfull[s], WQ_BYTES);
+                        const int2 wr = block_rows<MODE>(p, t, j);
+                        uint8_t* wq = sWq + s * WQ_BYTES;
+                        ptx::tma_load_2d(wq, &mapW, &wfull[s], kb * BK, wr.x);
+                        ptx::tma_load_2d(wq + WQ_BYTES / 2, &mapW3, &wfull[s], kb * BK, wr.y);
+                    }
+                if (!ok) break;
             }
             if (!ok) {
                 *s_abort = 1;
                 raise_error(p.status, MOE_ERR_DEVICE_TIMEOUT);
             }
-            for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
-                ptx::mbar_wait(&full[j % STAGES], (uint32_t)(j / STAGES) & 1u, nullptr);
+            for (int j = (it > WSTAGES ? it - WSTAGES : 0); j < it; ++j)
+                ptx::mbar_wait(&wfull[j % WSTAGES], (uint32_t)(j / WSTAGES) & 1u, nullptr);
         }
-    } else if (warp == 1) {
-        // -------------------------------------------------------- MMA issuer
+    } else if (warp == TOKP_WARP) {
+        // ----------------------------------- TMA producer (token chunks)
+        // Chunk = nmma rows x up to CH k-blocks of a segment; atom i = 2(kb -
+        // first kb of the chunk) + a (64 k each) at i * nmma * 128, 16-row
+        // boxes inside.
         if (lane == 0) {
-            int it = 0, tc = 0;
+            int cc = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++tc) {
-                const Tile t = tcffn::decode_tile<MODE, BM>(p, s_start, s_off, G, tile);
-                const int acc = tc & 1;
-                const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
-                if (!ptx::mbar_wait(&tempty[acc], aph ^ 1u, s_abort)) { ok = false; break; }
-                ptx::tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * MMA_N);
-                for (int kb = 0; kb < t.nk; ++kb, ++it) {
-                    const int s = it % STAGES, b = it % NB16;
-                    const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
-                    const uint32_t bph = (uint32_t)(it / NB16) & 1u;
-                    if (!ptx::mbar_wait(&full[s], ph, s_abort)) { ok = false; break; }
-                    if (!ptx::mbar_wait(&cfull[b], bph, s_abort)) { ok = false; break; }
-                    ptx::tc_fence_after();
-                    const uint64_t ad = ptx::sw128_desc(ptx::smem_u32(sA + s * A_BYTES));
-                    const uint64_t bd = ptx::sw128_desc(ptx::smem_u32(sB16 + b * B16_BYTES));
-#pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk)
-                        ptx::mma_bf16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2),
-                                      IDESC, (kb | kk) != 0 ? 1u : 0u);
-                    ptx::mma_commit(&empty[s]);
-                    ptx::mma_commit(&cempty[b]);
+            FOR_EACH_SEG(t)
+                const int atom = t.nmma * 128;
+                for (int kc = t.kb0; kc < t.kb1; kc += CH, ++cc) {
+                    const int kend = min(kc + CH, t.kb1);
+                    const int ub = cc & 1;
+                    if (!ptx::mbar_wait(&kempty[ub], ((uint32_t)(cc >> 1) & 1u) ^ 1u, s_abort)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::mbar_arrive_expect_tx(&kfull[ub], (uint32_t)((kend - kc) * 2 * atom));
+                    uint8_t* tb = sTok + ub * TB_BYTES;
+                    for (int kb = kc; kb < kend; ++kb)
+                        for (int a = 0; a < 2; ++a)
+                            for (int r = 0; r < t.nmma; r += TOK_BOX)
+                                ptx::tma_load_2d(tb + (2 * (kb - kc) + a) * atom + r * 128, &mapX,
+                                                 &kfull[ub], kb * BK + a * 64, t.tok0 + r);
                 }
                 if (!ok) break;
-                ptx::mma_commit(&tfull[acc]);
             }
             if (!ok) {
                 *s_abort = 1;
                 raise_error(p.status, MOE_ERR_DEVICE_TIMEOUT);
             }
-            ptx::mma_commit(drain);
-            ptx::mbar_wait(drain, 0, nullptr);
+            for (int j = (cc > 2 ? cc - 2 : 0); j < cc; ++j)
+                ptx::mbar_wait(&kfull[j & 1], (uint32_t)(j >> 1) & 1u, nullptr);
         }
-    } else if (warp >= 6) {
-        // -------------------------------------------------------- converters
-        // 256 weight rows x 8 chunks of 8 E4M3 bytes per stage; chunk c of row
-        // r becomes 16 f16 bytes at r*128 + ((c ^ (r & 7)) * 16), the 128-byte
-        // swizzle the MMA's operand descriptor expects.
-        const int ct = threadIdx.x - 6 * 32;
-        int it = 0;
-        bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-            const Tile t = tcffn::decode_tile<MODE, BM>(p, s_start, s_off, G, tile);
-            for (int kb = 0; kb < t.nk; ++kb, ++it) {
-                const int s = it % STAGES, b = it % NB16;
-                const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
-                const uint32_t bph = (uint32_t)(it / NB16) & 1u;
-                int w = 1;
-                if (lane == 0)
-                    w = ptx::mbar_wait(&full[s], ph, s_abort) &&
-                        ptx::mbar_wait(&cempty[b], bph ^ 1u, s_abort);
-                w = __shfl_sync(0xffffffffu, w, 0);
-                if (!w) { ok = false; break; }
-                const uint8_t* src = sBq + s * BQ_BYTES;
-                uint8_t* dst = sB16 + b * B16_BYTES;
-#pragma unroll 4
-                for (int i = 0; i < (MMA_N * 8) / CVT_THREADS; ++i) {
-                    const int j = ct + CVT_THREADS * i;
-                    const int r = j >> 3, c = j & 7;
-                    const uint2 q = *reinterpret_cast<const uint2*>(src + r * 64 + c * 8);
-                    const uint4 h = make_uint4(ptx::cvt_e4m3x2_f16x2((uint16_t)(q.x & 0xffffu)),
-                                               ptx::cvt_e4m3x2_f16x2((uint16_t)(q.x >> 16)),
-                                               ptx::cvt_e4m3x2_f16x2((uint16_t)(q.y & 0xffffu)),
-                                               ptx::cvt_e4m3x2_f16x2((uint16_t)(q.y >> 16)));
-                    *reinterpret_cast<uint4*>(dst + r * 128 + ((c ^ (r & 7)) << 4)) = h;
+    } else if (warp == 1 || warp >= MMA_WARP1) {
+        // ------------------------------------------------------- MMA issuers
+        // Issuer mi takes block mi of every tile (its A buffer, its
+        // accumulator).  An issuer without a block in a tile still arrives on
+        // the tile's shared barriers (token chunks, accumulators).
+        const int mi = warp == 1 ? 0 : warp - MMA_WARP1 + 1;
+        if (lane == 0) {
+            int n = 0, tc = 0, cc = 0;          // A-buffer fills, tiles, token chunks
+            bool ok = true;
+            const uint32_t a_tmem = tmem_base + (uint32_t)(A_COL0 + mi * A_COLS);
+            FOR_EACH_SEG(t)
+                const int acc = tc & 1;
+                const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
+                ++tc;
+                const bool mine = mi < t.nblk;
+                if (!ptx::mbar_wait(&tempty[acc], aph ^ 1u, s_abort)) { ok = false; break; }
+                ptx::tc_fence_after();
+                const uint32_t idesc = ptx::idesc_f16_f32(WROWS, t.nmma);
+                const int atom = t.nmma * 128;
+                const uint8_t* tb = sTok;
+                int kc = t.kb0;
+                for (int kb = t.kb0; ok && kb < t.kb1; ++kb) {
+                    if ((kb - t.kb0) % CH == 0) {                // next token chunk
+                        if (!ptx::mbar_wait(&kfull[cc & 1], (uint32_t)(cc >> 1) & 1u, s_abort)) {
+                            ok = false;
+                            break;
+                        }
+                        tb = sTok + (cc & 1) * TB_BYTES;
+                        kc = kb;
+                    }
+                    const uint64_t bd0 = ptx::sw128_desc(ptx::smem_u32(tb + (2 * (kb - kc)) * atom));
+                    const uint64_t bd1 =
+                        ptx::sw128_desc(ptx::smem_u32(tb + (2 * (kb - kc) + 1) * atom));
+                    const uint32_t first = kb > t.kb0 ? 1u : 0u;
+                    for (int j = mi; j < t.nblk; j += NISS) {
+                        if (!ptx::mbar_wait(&cfull[mi], (uint32_t)n & 1u, s_abort)) {
+                            ok = false;
+                            break;
+                        }
+                        ++n;
+                        ptx::tc_fence_after();
+                        const uint32_t d_tmem =
+                            tmem_base + (uint32_t)(acc * ACC_SET + j * TOK);
+                        ptx::mma_f16_tmem_a(d_tmem, a_tmem + 0, bd0 + 0, idesc, first);
+                        ptx::mma_f16_tmem_a(d_tmem, a_tmem + 8, bd0 + 2, idesc, 1u);
+                        ptx::mma_f16_tmem_a(d_tmem, a_tmem + 16, bd0 + 4, idesc, 1u);
+                        ptx::mma_f16_tmem_a(d_tmem, a_tmem + 24, bd0 + 6, idesc, 1u);
+                        ptx::mma_f16_tmem_a(d_tmem, a_tmem + 32, bd1 + 0, idesc, 1u);
+                        ptx::mma_f16_tmem_a(d_tmem, a_tmem + 40, bd1 + 2, idesc, 1u);
+                        ptx::mma_f16_tmem_a(d_tmem, a_tmem + 48, bd1 + 4, idesc, 1u);
+                        ptx::mma_f16_tmem_a(d_tmem, a_tmem + 56, bd1 + 6, idesc, 1u);
+                        ptx::mma_commit(&cempty[mi]);
+                    }
+                    if (ok && (kb + 1 == t.kb1 || (kb + 1 - t.kb0) % CH == 0)) {   // chunk done
+                        if (mine) ptx::mma_commit(&kempty[cc & 1]);
+                        else ptx::mbar_arrive(&kempty[cc & 1]);
+                        ++cc;
+                    }
                 }
-                ptx::fence_proxy_async_smem();
-                ptx::mbar_arrive(&cfull[b]);
+                if (!ok) break;
+                if (mine) ptx::mma_commit(&tfull[acc]);
+                else ptx::mbar_arrive(&tfull[acc]);
             }
+            if (!ok) {
+                *s_abort = 1;
+                raise_error(p.status, MOE_ERR_DEVICE_TIMEOUT);
+            }
+            ptx::mma_commit(&drain[mi]);
+            ptx::mbar_wait(&drain[mi], 0, nullptr);
+        }
+    } else if (warp >= 6 && warp < TOKP_WARP) {
+        // -------------------------------------------------------- converters
+        // Thread = weight row r (the warp's TMEM lane quadrant) and half h of
+        // the stage's K: chunks 4h .. 4h+3 of 16 codes, read at their swizzled
+        // places (c ^ (r & 7)), so that 8 consecutive rows hit 8 different
+        // bank groups; 64 codes -> 32 f16 pairs -> TMEM columns 32h .. 32h+31
+        // of the A buffer.
+        const int q = warp & 3, h = (warp - 6) >> 2;
+        const int r = q * 32 + lane;
+        const uint32_t a_lane = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(A_COL0 + h * 32);
+        int it = 0;
+        uint32_t nfill = 0;                      // bit j: parity of A buffer j's fills so far
+        bool ok = true;
+        FOR_EACH_SEG(t)
+            for (int kb = t.kb0; ok && kb < t.kb1; ++kb)
+                for (int j = 0; j < t.nblk; ++j, ++it) {
+                    const int s = it % WSTAGES, b = j;
+                    const uint32_t ph = (uint32_t)(it / WSTAGES) & 1u;
+                    const uint32_t bph = (nfill >> b) & 1u;
+                    nfill ^= 1u << b;
+                    if (!__all_sync(0xffffffffu, ptx::mbar_wait(&wfull[s], ph, s_abort))) {
+                        ok = false;
+                        break;
+                    }
+                    uint4 qv[4];
+                    const uint8_t* src = sWq + s * WQ_BYTES + r * 128;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        qv[i] = *reinterpret_cast<const uint4*>(src + (((4 * h + i) ^ (r & 7)) << 4));
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(&wempty[s]);     // codes are in registers
+                    if (!__all_sync(0xffffffffu, ptx::mbar_wait(&cempty[b], bph ^ 1u, s_abort))) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {         // 16 columns at a time
+                        uint32_t wv[16];
+#pragma unroll
+                        for (int i = 0; i < 2; ++i) {
+                            const uint4 c = qv[2 * hh + i];
+                            e4m3x4_to_f16x4_pow2(c.x, wv[8 * i + 0], wv[8 * i + 1]);
+                            e4m3x4_to_f16x4_pow2(c.y, wv[8 * i + 2], wv[8 * i + 3]);
+                            e4m3x4_to_f16x4_pow2(c.z, wv[8 * i + 4], wv[8 * i + 5]);
+                            e4m3x4_to_f16x4_pow2(c.w, wv[8 * i + 6], wv[8 * i + 7]);
+                        }
+                        ptx::tmem_st16(a_lane + (uint32_t)(b * A_COLS + hh * 16), wv);
+                    }
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(&cfull[b]);
+                }
+            if (!ok) break;
         }
         if (!ok && lane == 0) {
             *s_abort = 1;
             raise_error(p.status, MOE_ERR_DEVICE_TIMEOUT);
         }
-    } else {
+    } else if (warp >= 2 && warp < 6) {
         // ---------------------------------------------------------- epilogue
-        const int q = warp & 3;
-        const int row_in_tile = q * 32 + lane;
+        const int q = warp & 3;                  // TMEM lane quadrant
+        const int row = q * 32 + lane;           // weight row of the block
+        const int et = threadIdx.x - 64;
         int tc = 0;
-        for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++tc) {
-            const Tile t = tcffn::decode_tile<MODE, BM>(p, s_start, s_off, G, tile);
+        FOR_EACH_SEG(t)
             const int acc = tc & 1;
             const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
+            ++tc;
+            // inputs of the epilogue, while the tile's MMAs run: own row slots,
+            // and the token slots into the buffer of this tile's parity
+            prefetch_rows<MODE>(p, t, row, s_pre);
+            int* tok_a = s_tok_a + acc * TOK;
+            float* tok_w = s_tok_w + acc * TOK;
+            if (MODE == kModeDown) {
+                for (int c = et; c < t.ntok; c += 128) {
+                    const int a = p.perm_src[t.tok0 + c];
+                    tok_a[c] = a;
+                    tok_w[c] = p.gate_w[a];
+                }
+            }
             int ok = 1;
             if (lane == 0) ok = ptx::mbar_wait(&tfull[acc], aph, s_abort) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) {
-                if (lane == 0) {
-                    *s_abort = 1;
-                    raise_error(p.status, MOE_ERR_DEVICE_TIMEOUT);
-                }
+            // the four epilogue warps share named barriers below, so they take
+            // one decision: a snapshot of the abort flag between two barriers
+            if (lane == 0 && !ok) *s_abort = 1;
+            epi_bar();
+            if (et == 0) *s_go = *s_abort ? 0 : 1;
+            epi_bar();
+            if (!*s_go) {
+                if (et == 0) raise_error(p.status, MOE_ERR_DEVICE_TIMEOUT);
                 break;
             }
             ptx::tc_fence_after();
-            const uint32_t taddr = tmem_base + (uint32_t)(acc * MMA_N) + ((uint32_t)(q * 32) << 16);
-            epilogue_fp8<MODE>(p, t, taddr, t.arow + row_in_tile);
+            const uint32_t tq = tmem_base + (uint32_t)(acc * ACC_SET) + ((uint32_t)(q * 32) << 16);
+            if (t.c_first == t.c_last) {                     // the whole tile is ours
+                for (int j = 0; j < t.nblk; ++j) {
+                    __syncwarp();
+                    float v[32];
+                    ptx::tmem_ld32(tq + (uint32_t)(j * TOK), v);
+                    finish_block<MODE>(p, t, j, row, v, s_xch, s_pre, tok_a, tok_w);
+                }
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(&tempty[acc]);
+                continue;
+            }
+            // part of a shared tile: partial sums -> this CTA's slot
+            // (0 = the tile of its first segment, 1 = of its last), [block][column][row]
+            const int slot = (t.tile == t_first) ? 0 : 1;
+            float* mine = p.split_part + ((size_t)blockIdx.x * 2 + slot) * G * slot_floats;
+            for (int j = 0; j < t.nblk; ++j) {
+                __syncwarp();
+                float v[32];
+                ptx::tmem_ld32(tq + (uint32_t)(j * TOK), v);
+#pragma unroll
+                for (int c = 0; c < 32; ++c)
+                    if (c < t.ntok) mine[j * slot_floats + (size_t)c * WROWS + row] = v[c];
+            }
             ptx::tc_fence_before();
             ptx::mbar_arrive(&tempty[acc]);
+            __threadfence();
+            epi_bar();
+            if (et == 0) {
+                int parts = 0;                               // CTAs with work in the tile
+                for (int c = t.c_first; c <= t.c_last; ++c)
+                    parts += cta_start(W, grid, c) < cta_start(W, grid, c + 1);
+                const int prev = atomicAdd(p.split_ticket + t.c_last, 1);
+                const int last = prev == parts - 1;
+                if (last) p.split_ticket[t.c_last] = 0;      // ready for the next launch
+                *s_last = last;
+            }
+            epi_bar();
+            if (!*s_last) continue;
+            __threadfence();
+            for (int j = 0; j < t.nblk; ++j) {
+                float v[32];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) v[c] = 0.f;
+                for (int cta = t.c_first; cta <= t.c_last; ++cta) {
+                    const long long s0 = cta_start(W, grid, cta);
+                    if (s0 == cta_start(W, grid, cta + 1)) continue;        // no work there
+                    const int sl = (t.tile == (int)(s0 / nk)) ? 0 : 1;
+                    const float* src =
+                        p.split_part + ((size_t)cta * 2 + sl) * G * slot_floats + j * slot_floats;
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        if (c < t.ntok) v[c] += __ldcg(src + (size_t)c * WROWS + row);
+                }
+                finish_block<MODE>(p, t, j, row, v, s_xch, s_pre, tok_a, tok_w);
+            }
         }
     }
+#undef FOR_EACH_SEG
 
     ptx::tc_fence_before();
     __syncthreads();
@@ -361,7 +678,8 @@ cudaError_t launch_ffn_fp8(int mode, const CUtensorMap* maps, const TcFfnArgs& p
     const cudaError_t err =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (err != cudaSuccess) return err;
-    return launch_kernel(kernel, dim3(num_sms), dim3(NUM_THREADS), SMEM_BYTES, st, 1, maps[0],
+    const int grid = num_sms < kFp8MaxGrid ? num_sms : kFp8MaxGrid;
+    return launch_kernel(kernel, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, st, 1, maps[0],
                          maps[1], maps[2], p);
 }
 

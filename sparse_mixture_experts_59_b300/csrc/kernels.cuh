@@ -100,13 +100,22 @@ struct TcFfnArgs {
     int* status;
     const float* wscale;      // FP8 weights: per-row scales [E, N] (gate / fc1 / down)
     const float* wscale2;     // FP8 SwiGLU: up-projection scales [E, N]
+    int* split_ticket;        // FP8 split-K: per-tile counters, zero between launches
+    int split_tickets;        //   their number
+    float* split_part;        //   fp32 partial sums
+    long long split_bytes;    //   their capacity
 };
 int ffn_tc_smem_bytes();
 // maps: A, B, B2, A_sh, B_sh, B2_sh (see ffn_tc.cu)
 cudaError_t launch_ffn_tc(int mode, const CUtensorMap* maps, const TcFfnArgs& p, int num_sms,
                           cudaStream_t st);
-// ffn_fp8.cu: FP8 (E4M3) weights with per-row scales; maps: A (f16 rows),
-// B (E4M3 rows, no swizzle), B2 (E4M3 up rows for SwiGLU)
+// ffn_fp8.cu: FP8 (E4M3) weights with per-row scales, weights on the MMA's M;
+// at most kFp8MaxGrid CTAs (its partial-sum slots: 2 per CTA of 4 weight blocks
+// x 128 rows x 32 tokens fp32, and one ticket per CTA)
+// maps: X (f16 token rows, box 64 x 16), W and W3 (E4M3 rows, box 128 bytes x
+// 64 rows; W3 = W for GELU / down), all with the 128-byte swizzle
+constexpr int kFp8MaxGrid = 160;
+constexpr size_t kFp8SplitBytes = (size_t)2 * kFp8MaxGrid * 4 * 128 * 32 * 4;
 cudaError_t launch_ffn_fp8(int mode, const CUtensorMap* maps, const TcFfnArgs& p, int num_sms,
                            cudaStream_t st);
 // ffn_tc2.cu: the same on CTA pairs (cta_group::2), 256-row tiles; same maps
