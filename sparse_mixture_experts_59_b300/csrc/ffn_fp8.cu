@@ -47,11 +47,11 @@
 //               memory before its accumulators are ready: a global load waits
 //               several microseconds while the weight stream runs.
 //
-// The conversion is integer work, no float arithmetic: an E4M3 code with sign
-// s, exponent field e (bias 7) and mantissa m is, re-laid as an f16 bit
-// pattern (sign at bit 15, e at bits 13..10, m at bits 9..7), the f16 number
-// code * 2^-8 (f16 bias 15 = 7 + 8; E4M3 subnormals become f16 subnormals
-// with the same mantissa).  The 2^8 goes into the row scale, exactly.
+// Every E4M3 value (subnormals included, |v| <= 448) is an f16 value, so the
+// conversion (cvt.rn.f16x2.e4m3x2, two codes per instruction) is exact and the
+// products with the f16 tokens are exact in the fp32 accumulator.  (Measured:
+// the conversion instruction beats a bit re-layout on the integer pipe, which
+// needs 7 operations per 4 codes and leaves the converters ALU-bound.)
 //
 // Work balance (stream-K): the W = tiles x k-blocks units of work are cut into
 // one contiguous range per CTA.  A tile that lies in one range is finished
@@ -116,14 +116,11 @@ struct Fp8Traits {
     static constexpr int UNITS = MODE == kModeSwiglu ? 64 : 128;
 };
 
-// Four E4M3 codes (byte i = code i) -> four f16 equal to code * 2^-8, in two
+// Four E4M3 codes (byte i = code i) -> four f16 of the same values, in two
 // words (codes 0,1 in lo; 2,3 in hi; lower code in the lower half).
-// High byte of each f16: sign | e << 2 | m >> 1; low byte: (m & 1) << 7.
-__device__ __forceinline__ void e4m3x4_to_f16x4_pow2(uint32_t x, uint32_t& lo, uint32_t& hi) {
-    const uint32_t hb = (x & 0x80808080u) | ((x & 0x7e7e7e7eu) >> 1);
-    const uint32_t lb = (x & 0x01010101u) << 7;
-    lo = __byte_perm(lb, hb, 0x5140);
-    hi = __byte_perm(lb, hb, 0x7362);
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t x, uint32_t& lo, uint32_t& hi) {
+    lo = ptx::cvt_e4m3x2_f16x2((uint16_t)(x & 0xffffu));
+    hi = ptx::cvt_e4m3x2_f16x2((uint16_t)(x >> 16));
 }
 
 // Stream-K ranges: CTA c owns work units [cta_start(c), cta_start(c + 1)).
@@ -182,9 +179,9 @@ __device__ __forceinline__ int2 block_rows(const TcFfnArgs& p, const Seg& t, int
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 // Epilogue of one block's accumulator (tokens 0..31) for the calling thread's
-// weight row `row`; v holds the raw sums (weights at 2^-8 scale).
-// Row scales (times 2^8) and biases of the tile's blocks for the calling
-// thread's weight row, into its own slots of the prefetch area.
+// weight row `row`; v holds the sums over the unscaled codes.
+// Row scales and biases of the tile's blocks for the calling thread's weight
+// row, into its own slots of the prefetch area.
 template <int MODE>
 __device__ __forceinline__ void prefetch_rows(const TcFfnArgs& p, const Seg& t, int row,
                                               float* s_pre) {
@@ -194,11 +191,11 @@ __device__ __forceinline__ void prefetch_rows(const TcFfnArgs& p, const Seg& t, 
         float sc = 0.f, b = 0.f;
         if (MODE == kModeSwiglu) {
             const int u = u0 + (row & 63);
-            if (u < p.N) sc = 256.f * (row < 64 ? p.wscale : p.wscale2)[sbase + u];
+            if (u < p.N) sc = (row < 64 ? p.wscale : p.wscale2)[sbase + u];
         } else {
             const int n = u0 + row;
             if (n < p.N) {
-                sc = 256.f * p.wscale[sbase + n];
+                sc = p.wscale[sbase + n];
                 if (p.bias) b = __bfloat162float(p.bias[sbase + n]);
             }
         }
@@ -547,10 +544,10 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
 #pragma unroll
                         for (int i = 0; i < 2; ++i) {
                             const uint4 c = qv[2 * hh + i];
-                            e4m3x4_to_f16x4_pow2(c.x, wv[8 * i + 0], wv[8 * i + 1]);
-                            e4m3x4_to_f16x4_pow2(c.y, wv[8 * i + 2], wv[8 * i + 3]);
-                            e4m3x4_to_f16x4_pow2(c.z, wv[8 * i + 4], wv[8 * i + 5]);
-                            e4m3x4_to_f16x4_pow2(c.w, wv[8 * i + 6], wv[8 * i + 7]);
+                            e4m3x4_to_f16x4(c.x, wv[8 * i + 0], wv[8 * i + 1]);
+                            e4m3x4_to_f16x4(c.y, wv[8 * i + 2], wv[8 * i + 3]);
+                            e4m3x4_to_f16x4(c.z, wv[8 * i + 4], wv[8 * i + 5]);
+                            e4m3x4_to_f16x4(c.w, wv[8 * i + 6], wv[8 * i + 7]);
                         }
                         ptx::tmem_st16(a_lane + (uint32_t)(b * A_COLS + hh * 16), wv);
                     }

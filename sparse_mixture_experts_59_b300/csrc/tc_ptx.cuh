@@ -77,6 +77,14 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Two E4M3 floats (low byte first) -> two f16 packed in 32 bits; exact, as
+// every E4M3 value is an f16 value.
+__device__ __forceinline__ uint32_t cvt_e4m3x2_f16x2(uint16_t v) {
+    uint32_t out;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(out) : "h"(v));
+    return out;
+}
+
 // Instruction descriptor, kind::f16 with f16 A/B (format 0), fp32 accumulator.
 __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
     return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
