@@ -26,16 +26,18 @@
 // MMA read), which at 128 B/clock caps the weight stream near the HBM rate;
 // through TMEM it is 2 bytes.
 //
-// One CTA per SM, 576 threads:
+// One CTA per SM, 448 threads:
 //   warp 0      TMA: E4M3 weight rows (128 bytes of K, 128-byte swizzle) into
-//               a 9-stage ring that the converters release as soon as they
+//               a 10-stage ring that the converters release as soon as they
 //               hold a stage's codes in registers;
-//   warp 14     TMA: the tile's f16 token rows (128-byte swizzle) in chunks of
+//   warp 10     TMA: the tile's f16 token rows (128-byte swizzle) in chunks of
 //               up to 24 KB into two buffers, a chunk ahead;
-//   warps 6-13  converters, one thread per weight row and half of the stage's
-//               K: E4M3 -> f16 pairs in registers, tcgen05.st into the TMEM A
-//               buffer of the stage's block;
-//   warps 1, 15-17  MMA issuers, issuer i for block i of the tile:
+//   warps 6-9   converters, one per TMEM lane quadrant, thread = weight row:
+//               E4M3 -> f16 pairs in registers, tcgen05.st into the TMEM A
+//               buffer of the stage's block (a stage is released when the
+//               slowest converter warp has read it, so fewer warps, one per
+//               scheduler, keep the ring fuller than eight);
+//   warps 1, 11-13  MMA issuers, issuer i for block i of the tile:
 //               tcgen05.mma kind::f16 (M=128, N=tokens, K=16), A from its TMEM
 //               buffer, B (tokens) from shared memory, into the block's
 //               accumulator.  A thread issues a small MMA only every ~50-100
@@ -79,7 +81,7 @@ constexpr int G = 4;                           // weight blocks per tile
 constexpr int NISS = G;                        // MMA issuers and TMEM A buffers, one per block
 constexpr int TOK = 32;                        // tokens per tile at most (MMA N)
 constexpr int TOK_BOX = 16;                    // token rows per TMA box
-constexpr int WSTAGES = 9;                     // E4M3 weight ring
+constexpr int WSTAGES = 10;                    // E4M3 weight ring
 constexpr int TB_BYTES = 24 * 1024;            // token chunk buffer (two of them)
 constexpr int WQ_BYTES = WROWS * BK;           // E4M3 codes of one stage
 constexpr int A_COLS = BK / 2;                 // TMEM columns of one A buffer (f16 pairs)
@@ -87,7 +89,9 @@ constexpr int ACC_SET = G * TOK;               // TMEM columns of a tile's accum
 constexpr int A_COL0 = 2 * ACC_SET;            // two accumulator sets, then the A buffers
 constexpr int TMEM_COLS = 512;
 static_assert(A_COL0 + NISS * A_COLS <= TMEM_COLS, "tensor memory budget");
-constexpr int CVT_WARPS = 8;
+constexpr int CVT_WARPS = 4;                   // 4 or 8: one or two per TMEM lane quadrant
+constexpr int CVT_CHUNKS = 8 / (CVT_WARPS / 4);  // 16-code chunks per converter thread and stage
+static_assert(CVT_WARPS == 4 || CVT_WARPS == 8, "converter warps cover each lane quadrant");
 constexpr int TOKP_WARP = 6 + CVT_WARPS;      // token producer
 constexpr int MMA_WARP1 = TOKP_WARP + 1;      // issuers 1..NISS-1 (issuer 0: warp 1)
 constexpr int NUM_THREADS = (MMA_WARP1 + NISS - 1) * 32;
@@ -504,14 +508,15 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
         }
     } else if (warp >= 6 && warp < TOKP_WARP) {
         // -------------------------------------------------------- converters
-        // Thread = weight row r (the warp's TMEM lane quadrant) and half h of
-        // the stage's K: chunks 4h .. 4h+3 of 16 codes, read at their swizzled
-        // places (c ^ (r & 7)), so that 8 consecutive rows hit 8 different
-        // bank groups; 64 codes -> 32 f16 pairs -> TMEM columns 32h .. 32h+31
-        // of the A buffer.
+        // Thread = weight row r (the warp's TMEM lane quadrant) and part h of
+        // the stage's K: chunks h*CVT_CHUNKS .. of 16 codes, read at their
+        // swizzled places (c ^ (r & 7)), so that 8 consecutive rows hit 8
+        // different bank groups; chunk c -> 8 f16 pairs -> TMEM columns 8c ..
+        // 8c+7 of the A buffer.
         const int q = warp & 3, h = (warp - 6) >> 2;
         const int r = q * 32 + lane;
-        const uint32_t a_lane = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(A_COL0 + h * 32);
+        const uint32_t a_lane =
+            tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(A_COL0 + 8 * h * CVT_CHUNKS);
         int it = 0;
         uint32_t nfill = 0;                      // bit j: parity of A buffer j's fills so far
         bool ok = true;
@@ -526,11 +531,12 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
                         ok = false;
                         break;
                     }
-                    uint4 qv[4];
+                    uint4 qv[CVT_CHUNKS];
                     const uint8_t* src = sWq + s * WQ_BYTES + r * 128;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        qv[i] = *reinterpret_cast<const uint4*>(src + (((4 * h + i) ^ (r & 7)) << 4));
+                    for (int i = 0; i < CVT_CHUNKS; ++i)
+                        qv[i] = *reinterpret_cast<const uint4*>(
+                            src + (((CVT_CHUNKS * h + i) ^ (r & 7)) << 4));
                     __syncwarp();
                     if (lane == 0) ptx::mbar_arrive(&wempty[s]);     // codes are in registers
                     if (!__all_sync(0xffffffffu, ptx::mbar_wait(&cempty[b], bph ^ 1u, s_abort))) {
@@ -539,7 +545,7 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
                     }
                     ptx::tc_fence_after();
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {         // 16 columns at a time
+                    for (int hh = 0; hh < CVT_CHUNKS / 2; ++hh) {   // 16 columns at a time
                         uint32_t wv[16];
 #pragma unroll
                         for (int i = 0; i < 2; ++i) {
