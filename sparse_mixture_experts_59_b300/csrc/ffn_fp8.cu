@@ -313,18 +313,25 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
         ptx::tmem_alloc(s_tmem, TMEM_COLS);
         ptx::tmem_relinquish();
     }
-    pdl_wait();
+    // Only the token rows come from the kernel just before this one (the
+    // gather, or the up projection for the down projection): the offsets,
+    // slots and gate weights are older and the weights and scales are inputs.
+    // So the weight stream starts now, over the previous kernel's tail, and
+    // only the token producer waits for that kernel (pdl_wait below).  The
+    // partial-sum scratch, which the two projections share, is first touched
+    // by the epilogue, after MMAs that consumed waited-for tokens.
     pdl_trigger();
     for (int i = threadIdx.x; i <= p.E; i += NUM_THREADS) s_off[i] = p.offsets[i];
+    __syncthreads();
     const int nwb = (p.N + Fp8Traits<MODE>::UNITS - 1) / Fp8Traits<MODE>::UNITS;
     if (warp == 0) {            // longest segment: sizes the token chunks
         int m = 0;
-        for (int g = lane; g < p.E; g += 32) m = max(m, p.offsets[g + 1] - p.offsets[g]);
+        for (int g = lane; g < p.E; g += 32) m = max(m, s_off[g + 1] - s_off[g]);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
         if (lane == 0) *s_maxrows = m;
     }
-    group_tile_prefix(p.offsets, p.E, 0, TOK, (nwb + G - 1) / G, 0, s_start);
+    group_tile_prefix(s_off, p.E, 0, TOK, (nwb + G - 1) / G, 0, s_start);
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
@@ -408,6 +415,7 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
         // first kb of the chunk) + a (64 k each) at i * nmma * 128, 16-row
         // boxes inside.
         if (lane == 0) {
+            pdl_wait();                          // the token rows are the previous kernel's
             int cc = 0;
             bool ok = true;
             FOR_EACH_SEG(t)
