@@ -26,23 +26,25 @@
 // MMA read), which at 128 B/clock caps the weight stream near the HBM rate;
 // through TMEM it is 2 bytes.
 //
-// One CTA per SM, 448 threads:
+// One CTA per SM, 384 threads; the warps that issue TMA or MMA instructions
+// sit on different schedulers (warp % 4), as issuing them slows the other
+// warps of the scheduler (measured: a converter warp sharing its scheduler
+// with two MMA issuers ran ~2400 clocks behind one sharing with none, and the
+// slowest converter gates both the weight ring and the MMAs):
 //   warp 0      TMA: E4M3 weight rows (128 bytes of K, 128-byte swizzle) into
 //               a 10-stage ring that the converters release as soon as they
 //               hold a stage's codes in registers;
-//   warp 10     TMA: the tile's f16 token rows (128-byte swizzle) in chunks of
-//               up to 24 KB into two buffers, a chunk ahead;
+//   warp 1      TMEM owner; TMA: the tile's f16 token rows (128-byte swizzle)
+//               in chunks of up to 24 KB into two buffers, a chunk ahead;
 //   warps 6-9   converters, one per TMEM lane quadrant, thread = weight row:
 //               E4M3 -> f16 pairs in registers, tcgen05.st into the TMEM A
-//               buffer of the stage's block (a stage is released when the
-//               slowest converter warp has read it, so fewer warps, one per
-//               scheduler, keep the ring fuller than eight);
-//   warps 1, 11-13  MMA issuers, issuer i for block i of the tile:
-//               tcgen05.mma kind::f16 (M=128, N=tokens, K=16), A from its TMEM
-//               buffer, B (tokens) from shared memory, into the block's
-//               accumulator.  A thread issues a small MMA only every ~50-100
-//               clocks, and a stage needs 8, so one issuer could not keep up
-//               with the weight stream; warp 1 also owns the TMEM allocation;
+//               buffer of the stage's block;
+//   warps 10-11 MMA issuers, issuer i for blocks i and i + 2 of the tile:
+//               tcgen05.mma kind::f16 (M=128, N=tokens, K=16), A from the
+//               block's TMEM buffer, B (tokens) from shared memory, into the
+//               block's accumulator.  A thread issues a small MMA only every
+//               ~50-100 clocks and a stage needs 8, so one issuer could not
+//               keep up with the weight stream;
 //   warps 2-5   epilogue: row scales, fused activation / gate scale, f16 H
 //               (A operand of the down GEMM) or bf16 slot outputs.  The
 //               scales, biases and token slots of a tile are copied to shared
@@ -78,7 +80,7 @@ namespace {
 constexpr int BK = 128;                        // K per stage: one 128-byte row of codes
 constexpr int WROWS = 128;                     // weight rows per block (MMA M, TMEM lanes)
 constexpr int G = 4;                           // weight blocks per tile
-constexpr int NISS = G;                        // MMA issuers and TMEM A buffers, one per block
+constexpr int NISS = 2;                        // MMA issuers, blocks i, i + NISS, ...
 constexpr int TOK = 32;                        // tokens per tile at most (MMA N)
 constexpr int TOK_BOX = 16;                    // token rows per TMA box
 constexpr int WSTAGES = 10;                    // E4M3 weight ring
@@ -88,13 +90,14 @@ constexpr int A_COLS = BK / 2;                 // TMEM columns of one A buffer (
 constexpr int ACC_SET = G * TOK;               // TMEM columns of a tile's accumulators
 constexpr int A_COL0 = 2 * ACC_SET;            // two accumulator sets, then the A buffers
 constexpr int TMEM_COLS = 512;
-static_assert(A_COL0 + NISS * A_COLS <= TMEM_COLS, "tensor memory budget");
+static_assert(A_COL0 + G * A_COLS <= TMEM_COLS, "tensor memory budget (an A buffer per block)");
 constexpr int CVT_WARPS = 4;                   // 4 or 8: one or two per TMEM lane quadrant
 constexpr int CVT_CHUNKS = 8 / (CVT_WARPS / 4);  // 16-code chunks per converter thread and stage
 static_assert(CVT_WARPS == 4 || CVT_WARPS == 8, "converter warps cover each lane quadrant");
-constexpr int TOKP_WARP = 6 + CVT_WARPS;      // token producer
-constexpr int MMA_WARP1 = TOKP_WARP + 1;      // issuers 1..NISS-1 (issuer 0: warp 1)
-constexpr int NUM_THREADS = (MMA_WARP1 + NISS - 1) * 32;
+constexpr int TOKP_WARP = 1;                   // token producer (and TMEM owner)
+constexpr int MMA_WARP0 = 6 + CVT_WARPS;       // first MMA issuer
+constexpr int NUM_THREADS = (MMA_WARP0 + NISS) * 32;
+static_assert(MMA_WARP0 % 4 == 2 && NISS == 2, "issuers on schedulers 2 and 3");
 constexpr int XCH_LD = 33;
 
 constexpr int OFF_TOK = 0;
@@ -104,7 +107,7 @@ constexpr int OFF_PRE = OFF_XCH + 64 * XCH_LD * 4;   // [2][G][128] row scales, 
 constexpr int OFF_TOKA = OFF_PRE + 2 * G * WROWS * 4;
 constexpr int OFF_TOKW = OFF_TOKA + 2 * TOK * 4;     // token slots and weights, 2 buffers
 constexpr int OFF_BAR = OFF_TOKW + 2 * TOK * 4;
-constexpr int NUM_BARS = 2 * WSTAGES + 2 + 2 + 2 * NISS + 2 + 2 + NISS;
+constexpr int NUM_BARS = 2 * WSTAGES + 2 + 2 + 2 * G + 2 + 2 + NISS;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int OFF_START = OFF_MISC + 32;
 constexpr int OFF_OFFS = OFF_START + (kMaxExperts + 2) * 4;
@@ -271,9 +274,9 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
     uint64_t* wempty = wfull + WSTAGES;          // converters hold the codes
     uint64_t* kfull = wempty + WSTAGES;          // a token chunk landed
     uint64_t* kempty = kfull + 2;                // the issuers done with the chunk
-    uint64_t* cfull = kempty + 2;                // converted weights in issuer i's A buffer
-    uint64_t* cempty = cfull + NISS;             // issuer i's MMAs done with it
-    uint64_t* tfull = cempty + NISS;             // the issuers' accumulators complete
+    uint64_t* cfull = kempty + 2;                // converted weights in block j's A buffer
+    uint64_t* cempty = cfull + G;                // block j's MMAs done with it
+    uint64_t* tfull = cempty + G;                // the issuers' accumulators complete
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;                // per issuer
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
@@ -294,7 +297,7 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
             ptx::mbar_init(&kfull[s], 1);
             ptx::mbar_init(&kempty[s], NISS);
         }
-        for (int b = 0; b < NISS; ++b) {
+        for (int b = 0; b < G; ++b) {
             ptx::mbar_init(&cfull[b], CVT_WARPS);
             ptx::mbar_init(&cempty[b], 1);
         }
@@ -444,16 +447,17 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
             for (int j = (cc > 2 ? cc - 2 : 0); j < cc; ++j)
                 ptx::mbar_wait(&kfull[j & 1], (uint32_t)(j >> 1) & 1u, nullptr);
         }
-    } else if (warp == 1 || warp >= MMA_WARP1) {
+    } else if (warp >= MMA_WARP0) {
         // ------------------------------------------------------- MMA issuers
-        // Issuer mi takes block mi of every tile (its A buffer, its
-        // accumulator).  An issuer without a block in a tile still arrives on
-        // the tile's shared barriers (token chunks, accumulators).
-        const int mi = warp == 1 ? 0 : warp - MMA_WARP1 + 1;
+        // Issuer mi takes blocks mi, mi + NISS, ... of every tile (their A
+        // buffers and accumulators).  An issuer without a block in a tile
+        // still arrives on the tile's shared barriers (token chunks,
+        // accumulators).
+        const int mi = warp - MMA_WARP0;
         if (lane == 0) {
-            int n = 0, tc = 0, cc = 0;          // A-buffer fills, tiles, token chunks
+            uint32_t nfill = 0;                 // bit j: parity of block j's fills so far
+            int tc = 0, cc = 0;                 // tiles, token chunks
             bool ok = true;
-            const uint32_t a_tmem = tmem_base + (uint32_t)(A_COL0 + mi * A_COLS);
             FOR_EACH_SEG(t)
                 const int acc = tc & 1;
                 const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
@@ -479,14 +483,15 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
                         ptx::sw128_desc(ptx::smem_u32(tb + (2 * (kb - kc) + 1) * atom));
                     const uint32_t first = kb > t.kb0 ? 1u : 0u;
                     for (int j = mi; j < t.nblk; j += NISS) {
-                        if (!ptx::mbar_wait(&cfull[mi], (uint32_t)n & 1u, s_abort)) {
+                        if (!ptx::mbar_wait(&cfull[j], (nfill >> j) & 1u, s_abort)) {
                             ok = false;
                             break;
                         }
-                        ++n;
+                        nfill ^= 1u << j;
                         ptx::tc_fence_after();
                         const uint32_t d_tmem =
                             tmem_base + (uint32_t)(acc * ACC_SET + j * TOK);
+                        const uint32_t a_tmem = tmem_base + (uint32_t)(A_COL0 + j * A_COLS);
                         ptx::mma_f16_tmem_a(d_tmem, a_tmem + 0, bd0 + 0, idesc, first);
                         ptx::mma_f16_tmem_a(d_tmem, a_tmem + 8, bd0 + 2, idesc, 1u);
                         ptx::mma_f16_tmem_a(d_tmem, a_tmem + 16, bd0 + 4, idesc, 1u);
@@ -495,7 +500,7 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
                         ptx::mma_f16_tmem_a(d_tmem, a_tmem + 40, bd1 + 2, idesc, 1u);
                         ptx::mma_f16_tmem_a(d_tmem, a_tmem + 48, bd1 + 4, idesc, 1u);
                         ptx::mma_f16_tmem_a(d_tmem, a_tmem + 56, bd1 + 6, idesc, 1u);
-                        ptx::mma_commit(&cempty[mi]);
+                        ptx::mma_commit(&cempty[j]);
                     }
                     if (ok && (kb + 1 == t.kb1 || (kb + 1 - t.kb0) % CH == 0)) {   // chunk done
                         if (mine) ptx::mma_commit(&kempty[cc & 1]);
@@ -514,7 +519,7 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
             ptx::mma_commit(&drain[mi]);
             ptx::mbar_wait(&drain[mi], 0, nullptr);
         }
-    } else if (warp >= 6 && warp < TOKP_WARP) {
+    } else if (warp >= 6) {
         // -------------------------------------------------------- converters
         // Thread = weight row r (the warp's TMEM lane quadrant) and part h of
         // the stage's K: chunks h*CVT_CHUNKS .. of 16 codes, read at their
