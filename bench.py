@@ -53,6 +53,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--fp8", action="store_true",
+                    help="the main workload with FP8 E4M3 expert weights (profiling cases)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--sweep", default=None,
                     help="comma-separated token counts: time the layer at each T on the "
@@ -273,6 +275,12 @@ def run_ours(args, world, rank, local):
     peaks, peak_src = measured_peaks()
     cfg = workload_config(args)
     inp = workloads.make_inputs(cfg, device=dev)
+    bf16_inp = inp
+    if args.fp8:
+        inp = workloads.quantize_experts_fp8(inp)
+        cfg = inp["cfg"]
+        if args.no_decode:
+            bf16_inp = None                      # only the FP8 copy stays on the device
     layer = binding.MoeLayer(cfg, inp, device=dev)
     x = inp["x"]
     outputs = {"y": torch.empty_like(x), "counts_kept": torch.empty(cfg["E"], dtype=torch.int32,
@@ -304,13 +312,14 @@ def run_ours(args, world, rank, local):
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16, e4m3 expert weights" if args.fp8 else "bf16",
         "data": "synthetic: seeded x~N(0,1), expert weights~N(0,0.02), router~N(0,1/sqrt(d)); bf16",
         "config": {"workload": args.workload, "T": cfg["T"], "d_model": cfg["d"], "d_ff": cfg["F"],
                    "experts": cfg["E"], "top_k": cfg["k"], "act": cfg["act"],
                    "capacity": "dropless" if not cfg["capacity_factor"] else cfg["capacity_factor"],
                    "l2": "inputs larger than L2 (expert weights %.2f GB vs 126 MB L2); no flush"
-                         % (sum(inp[k].numel() * 2 for k in ("W1", "W3", "W2")
+                         % (sum(inp[k].numel() * inp[k].element_size() for k in ("W1", "W3", "W2")
                                 if inp.get(k) is not None) / 1e9),
                    "parallelism": "replicas" if world > 1 else "single",
                    "gemm_kernel": args.gemm or "auto"},
@@ -330,8 +339,8 @@ def run_ours(args, world, rank, local):
     if not args.no_e2e:
         result["e2e"] = run_e2e(layer, cfg, x, args, world, dev)
     if not args.no_decode:
-        result["decode"] = run_decode(args, inp, world, dev, peaks, peak_src)
-        result["decode_fp8"] = run_decode(args, inp, world, dev, peaks, peak_src, fp8=True)
+        result["decode"] = run_decode(args, bf16_inp, world, dev, peaks, peak_src)
+        result["decode_fp8"] = run_decode(args, bf16_inp, world, dev, peaks, peak_src, fp8=True)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(inp, cfg, args.cpu_seconds)
     del layer

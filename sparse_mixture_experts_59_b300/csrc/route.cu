@@ -99,8 +99,21 @@ router_topk_kernel(const float* part, int nsplit, const float* __restrict__ bias
         for (int j = 0; j < VPL; ++j) {
             const int e = lane + 32 * j;
             if (e < E) {
-                float v = part[(size_t)t * E + e];
-                for (int sp = 1; sp < nsplit; ++sp) v += part[((size_t)sp * Ttok + t) * E + e];
+                // the split-K partials, 8 loads in flight: accumulator a takes
+                // splits a, a+8, ...; combined in a fixed order (deterministic)
+                float acc[8];
+#pragma unroll
+                for (int a = 0; a < 8; ++a) acc[a] = 0.f;
+                const size_t stride = (size_t)Ttok * E;
+                const float* src = part + (size_t)t * E + e;
+                int sp = 0;
+                for (; sp + 8 <= nsplit; sp += 8) {
+#pragma unroll
+                    for (int a = 0; a < 8; ++a) acc[a] += src[(size_t)(sp + a) * stride];
+                }
+                for (int a = 0; sp + a < nsplit; ++a) acc[a] += src[(size_t)(sp + a) * stride];
+                float v = ((acc[0] + acc[1]) + (acc[2] + acc[3])) +
+                          ((acc[4] + acc[5]) + (acc[6] + acc[7]));
                 if (bias) v += bias[e];
                 if (write_logits) logits[(size_t)t * E + e] = v;
                 l[j] = v;

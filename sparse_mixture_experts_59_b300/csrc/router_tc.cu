@@ -161,7 +161,9 @@ RouterPlan router_tc_plan(int T, int d, int E) {
     p.NB = (E + 15) / 16 * 16;
     p.m_tiles = (T + BM - 1) / BM;
     p.nkb = (d + BK - 1) / BK;
-    const int target = 2 * 148;     // about two CTAs per SM stream x at once
+    // about two CTAs per SM stream x at once; few tokens (one or two M tiles)
+    // take at most 16 splits, as the top-k kernel adds the partials per token
+    const int target = p.m_tiles <= 2 ? 16 * p.m_tiles : 2 * 148;
     int splits = (target + p.m_tiles - 1) / p.m_tiles;
     if (splits > p.nkb) splits = p.nkb;
     if (splits < 1) splits = 1;
