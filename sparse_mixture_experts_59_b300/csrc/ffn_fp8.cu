@@ -71,7 +71,7 @@
 #include "common.cuh"
 #include "kernels.cuh"
 #include "launch.cuh"
-#include "tc_ptx.cuh"
+#include "tc_lowbit.cuh"
 
 namespace moe {
 
