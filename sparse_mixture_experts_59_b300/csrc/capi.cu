@@ -642,7 +642,8 @@ static int layer_forward_impl(const moe_cfg* cfg, const void* x, const void* Wr,
     if (ev) MOE_CUDA(cudaEventRecord(ev[2], st), "event record");
     MOE_TRY(run_expert_ffn(c, di, x, perm_src, offsets, topk_w, *w, Ys, Sh, ws, st,
                            ev ? ev + 3 : nullptr));
-    MOE_CUDA(launch_combine(c.dtype, x, Ys, drop, Sh, out->y, c.T, c.d, c.k, di.num_sms, st),
+    MOE_CUDA(launch_combine(c.dtype, x, Ys, drop, Sh, out->y, c.T, c.d, c.k, di.num_sms, st,
+                            c.capacity_factor > 0.f),
              "combine launch");
     if (ev) MOE_CUDA(cudaEventRecord(ev[6], st), "event record");
     return MOE_OK;

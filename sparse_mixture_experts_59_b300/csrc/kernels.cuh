@@ -62,9 +62,10 @@ cudaError_t launch_gather(int dtype, const void* x, const int* perm_src, const i
 // bf16 x -> f16 gathered rows (the FP8-weight path's token operand)
 cudaError_t launch_gather_f16(const void* x, const int* perm_src, const int* offsets, int E, int k,
                               int T, int d, void* Xp, int* status, int num_sms, cudaStream_t st);
+// use_mask = false: nothing was dropped (dropless layer), drop_mask is not read
 cudaError_t launch_combine(int dtype, const void* x, const void* Ys, const unsigned char* drop_mask,
                            const void* Sh, void* y, int T, int d, int k, int num_sms,
-                           cudaStream_t st);
+                           cudaStream_t st, bool use_mask = true);
 
 // ffn_simt.cu (fp32)
 struct SimtFfnArgs {

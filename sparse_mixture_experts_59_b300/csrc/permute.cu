@@ -75,7 +75,11 @@ gather_rows_f16_kernel(const uint4* __restrict__ x, const int* __restrict__ perm
 
 // y[t] = x[t] + sum_{s kept} Ys[t*k+s] (+ Sh[t]); fp32 sum in slot order, then
 // the shared expert, then the residual, rounded once.
-template <typename T>
+// y[t] = x[t] + sum over kept slots of Ys[t*k+s] (+ Sh[t]), fp32, one rounding.
+// USE_MASK = false for dropless layers (nothing is dropped): every load of a
+// vector is then independent and issued at once; with a mask, the slot loads
+// wait for the mask bytes (a dropped slot's row is never read).
+template <typename T, bool USE_MASK>
 __global__ void __launch_bounds__(256)
 combine_kernel(const T* __restrict__ x, const T* __restrict__ Ys,
                const unsigned char* __restrict__ drop_mask, const T* __restrict__ Sh,
@@ -89,12 +93,13 @@ combine_kernel(const T* __restrict__ x, const T* __restrict__ Ys,
          i += (long long)gridDim.x * blockDim.x) {
         const int t = (int)(i / vec_per_row);
         const int v = (int)(i - (long long)t * vec_per_row);
+        const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * d) + v);
         float acc[NV];
 #pragma unroll
         for (int j = 0; j < NV; ++j) acc[j] = 0.f;
         for (int s = 0; s < k; ++s) {
             const long long a = (long long)t * k + s;
-            if (drop_mask[a]) continue;
+            if (USE_MASK && drop_mask[a]) continue;
             float f[NV];
             unpack16(__ldg(reinterpret_cast<const uint4*>(Ys + a * d) + v), f);
 #pragma unroll
@@ -107,7 +112,7 @@ combine_kernel(const T* __restrict__ x, const T* __restrict__ Ys,
             for (int j = 0; j < NV; ++j) acc[j] += f[j];
         }
         float xf[NV];
-        unpack16(__ldg(reinterpret_cast<const uint4*>(x + (size_t)t * d) + v), xf);
+        unpack16(xv, xf);
 #pragma unroll
         for (int j = 0; j < NV; ++j) acc[j] += xf[j];
         reinterpret_cast<uint4*>(y + (size_t)t * d)[v] = pack16(acc);
@@ -140,19 +145,21 @@ cudaError_t launch_gather_f16(const void* x, const int* perm_src, const int* off
 
 cudaError_t launch_combine(int dtype, const void* x, const void* Ys, const unsigned char* drop_mask,
                            const void* Sh, void* y, int T, int d, int k, int num_sms,
-                           cudaStream_t st) {
+                           cudaStream_t st, bool use_mask) {
     const int esize = dtype == MOE_F32 ? 4 : 2;
     const long long total = (long long)T * (d * esize / 16);
     long long blocks = (total + 255) / 256;
     if (blocks > num_sms * 16) blocks = num_sms * 16;
     if (blocks < 1) blocks = 1;
     if (dtype == MOE_F32)
-        return launch_kernel(combine_kernel<float>, dim3((unsigned)blocks), dim3(256), 0, st, 1,
-                             (const float*)x, (const float*)Ys, drop_mask, (const float*)Sh,
-                             (float*)y, T, d, k);
-    return launch_kernel(combine_kernel<__nv_bfloat16>, dim3((unsigned)blocks), dim3(256), 0, st, 1,
-                         (const __nv_bfloat16*)x, (const __nv_bfloat16*)Ys, drop_mask,
-                         (const __nv_bfloat16*)Sh, (__nv_bfloat16*)y, T, d, k);
+        return launch_kernel(use_mask ? combine_kernel<float, true> : combine_kernel<float, false>,
+                             dim3((unsigned)blocks), dim3(256), 0, st, 1, (const float*)x,
+                             (const float*)Ys, drop_mask, (const float*)Sh, (float*)y, T, d, k);
+    return launch_kernel(use_mask ? combine_kernel<__nv_bfloat16, true>
+                                  : combine_kernel<__nv_bfloat16, false>,
+                         dim3((unsigned)blocks), dim3(256), 0, st, 1, (const __nv_bfloat16*)x,
+                         (const __nv_bfloat16*)Ys, drop_mask, (const __nv_bfloat16*)Sh,
+                         (__nv_bfloat16*)y, T, d, k);
 }
 
 }  // namespace moe
