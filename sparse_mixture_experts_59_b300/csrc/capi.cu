@@ -32,7 +32,8 @@ size_t esize(const moe_cfg& c) { return c.dtype == MOE_F32 ? 4 : 2; }
 size_t align_up(size_t v) { return (v + 255) & ~(size_t)255; }
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-constexpr int kRouterTopkMaxBlocks = 148;   // P partial sums to add up at the end
+constexpr int kRouterTopkMaxBlocks = 1024;  // one token per warp up to T = 8192; P partials
+                                            // of the blocks are added at the end
 int router_blocks(int T) {
     const int b = (T + 7) / 8;
     return b < 1 ? 1 : (b > kRouterTopkMaxBlocks ? kRouterTopkMaxBlocks : b);
