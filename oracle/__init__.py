@@ -14,7 +14,7 @@ import numpy as np
 
 from . import build as _build
 
-ORC_F32, ORC_BF16, ORC_E4M3 = 0, 1, 2
+ORC_F32, ORC_BF16, ORC_E4M3, ORC_E2M1P = 0, 1, 2, 3
 ORC_GELU_ERF, ORC_SWIGLU = 0, 1
 
 _lib = None
@@ -39,6 +39,8 @@ def _load():
         lib.oracle_layer_tokens_q.argtypes = [I, P, I, I, I, I, I, I, I, P, P, P, P, P, P,
                                               P, P, P, I, P, P, P, P, P, P, P, P, P]
         lib.oracle_e4m3_value.argtypes = [ctypes.c_uint]
+        lib.oracle_e2m1_value.argtypes = [ctypes.c_uint]
+        lib.oracle_e2m1_value.restype = ctypes.c_double
         lib.oracle_e4m3_value.restype = D
         lib.oracle_aux_loss.argtypes = [I, I, P, P]
         lib.oracle_aux_loss.restype = D
@@ -62,7 +64,8 @@ def _buf(a):
     """(contiguous numpy array, dtype code) for fp32 or bf16 data.
 
     Accepts numpy float32, numpy uint16 holding bf16 bit patterns, or CPU torch
-    tensors of dtype float32 / bfloat16 (viewed, not converted)."""
+    tensors of dtype float32 / bfloat16 (viewed, not converted); float8_e4m3fn
+    tensors are E4M3 codes and uint8 tensors the packed 4-bit weight layout."""
     if a is None:
         return None, None
     try:
@@ -75,6 +78,8 @@ def _buf(a):
                 return np.ascontiguousarray(a.numpy()), ORC_F32
             if a.dtype == torch.float8_e4m3fn:
                 return np.ascontiguousarray(a.view(torch.uint8).numpy()), ORC_E4M3
+            if a.dtype == torch.uint8:
+                return np.ascontiguousarray(a.numpy()), ORC_E2M1P
             raise TypeError("oracle takes float32 or bfloat16 tensors, got %s" % a.dtype)
     except ImportError:
         pass
@@ -83,11 +88,18 @@ def _buf(a):
         return a, ORC_F32
     if a.dtype == np.uint16:
         return a, ORC_BF16
+    if a.dtype == np.uint8:
+        return a, ORC_E2M1P
     raise TypeError("oracle takes float32 or bf16 (uint16 bits) arrays, got %s" % a.dtype)
 
 
 def _ptr(a):
     return None if a is None else ctypes.c_void_p(a.ctypes.data)
+
+
+def e2m1_value(code: int) -> float:
+    """The oracle's decoding of one E2M1 nibble (from the format's definition)."""
+    return float(_load().oracle_e2m1_value(int(code)))
 
 
 def e4m3_value(code: int) -> float:
@@ -213,7 +225,7 @@ def layer_tokens(inp, topk_idx, topk_w, drop_mask, tokens, want_slots=False,
     scales = []
     for key in ("s1", "s3", "s2"):
         v = inp.get(key)
-        if v is not None and wc == ORC_E4M3:
+        if v is not None and wc in (ORC_E4M3, ORC_E2M1P):
             try:
                 import torch
                 if isinstance(v, torch.Tensor):

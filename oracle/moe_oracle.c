@@ -54,7 +54,7 @@
 #include <string.h>
 #include <unistd.h>
 
-enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_E4M3 = 2 };
+enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_E4M3 = 2, ORC_E2M1P = 3 };
 enum { ORC_GELU_ERF = 0, ORC_SWIGLU = 1 };
 enum { ORC_SOFTMAX = 0, ORC_SIGMOID = 1 };
 
@@ -74,6 +74,39 @@ double oracle_e4m3_value(unsigned code)
     return sgn ? -v : v;
 }
 
+/* E2M1 (FP4: 1 sign, 2 exponent bits with bias 1, 1 mantissa bit): e = 0 gives
+ * (-1)^s m/2 (0 and 0.5); otherwise (-1)^s 2^(e-1) (1 + m/2), so the
+ * magnitudes are 0, 0.5, 1, 1.5, 2, 3, 4, 6.  The format has no infinity or NaN. */
+double oracle_e2m1_value(unsigned code)
+{
+    const int sgn = (code >> 3) & 1, e = (code >> 1) & 3, m = code & 1;
+    const double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return sgn ? -v : v;
+}
+
+/* Packed 4-bit weights (ORC_E2M1P), the 4-bit variant of "Quantization for
+ * MoE": each row of K values (K a multiple of 128) is stored as K/128 chunks
+ * of 80 bytes -- 64 bytes of E2M1 codes (value 2i of the chunk in the low
+ * nibble of byte i, value 2i+1 in the high nibble), then 8 E4M3 block scales
+ * (scale b multiplies values 16b .. 16b+15 of the chunk), then 8 zero bytes.
+ * The stored value is code * block scale; the row scale applies on top. */
+static double orc_load_e2m1p(const unsigned char *row, int col)
+{
+    const unsigned char *chunk = row + (size_t)(col / 128) * 80;
+    const int w = col % 128;
+    const unsigned byte = chunk[w / 2];
+    const unsigned code = (w & 1) ? (byte >> 4) : (byte & 15);
+    return oracle_e2m1_value(code) * oracle_e4m3_value(chunk[64 + w / 16]);
+}
+
+/* Bytes of one stored row of K weights. */
+static size_t orc_row_bytes(int K, int dtype)
+{
+    if (dtype == ORC_E2M1P)
+        return (size_t)(K / 128) * 80;
+    return (size_t)K * (dtype == ORC_F32 ? 4 : dtype == ORC_BF16 ? 2 : 1);
+}
+
 /* Exact widening of one stored element to double.  bf16 is the upper half of
  * an IEEE binary32 pattern. */
 static double orc_load(const void *base, size_t i, int dtype)
@@ -86,6 +119,14 @@ static double orc_load(const void *base, size_t i, int dtype)
     float f;
     memcpy(&f, &bits, sizeof f);
     return (double)f;
+}
+
+/* Element (row, col) of a weight matrix with K values per row. */
+static double orc_load_w(const void *base, size_t row, int col, int K, int dtype)
+{
+    if (dtype == ORC_E2M1P)
+        return orc_load_e2m1p((const unsigned char *)base + row * orc_row_bytes(K, dtype), col);
+    return orc_load(base, row * (size_t)K + col, dtype);
 }
 
 /* ---------------------------------------------------------------- threads */
@@ -298,10 +339,11 @@ int oracle_dispatch(int T, int k, int E, long long cap, const int *topk_idx,
  * SwiGLU ([S]): out = W2 . (silu(W1 . x) * (W3 . x)), silu(z) = z/(1+exp(-z)).
  * W1, W3 hold one row of d per hidden unit ([F, d]); W2 holds one row of F per
  * output ([d, F]) -- the nn.Linear weight layout.  b1 [F], b2 [d] optional.
- * Weights are stored in wdtype, biases in bdtype.  With E4M3 weights, s1, s3
- * [F] and s2 [d] are the per-row scales: row f of W1 is s1[f] * W1[f,:]
- * ("How Mixture of Experts Works", "Quantization for MoE"); each row's scale
- * multiplies its dot product.  h is caller scratch of F doubles. */
+ * Weights are stored in wdtype, biases in bdtype.  With E4M3 or packed E2M1
+ * weights, s1, s3 [F] and s2 [d] are the per-row scales: row f of W1 is
+ * s1[f] * W1[f,:] ("How Mixture of Experts Works", "Quantization for MoE");
+ * each row's scale multiplies its dot product.  h is caller scratch of F
+ * doubles. */
 void oracle_expert_ffn_q(int d, int F, int act, int wdtype, int bdtype, const double *xv,
                          const void *W1, const void *W3, const void *W2, const void *b1,
                          const void *b2, const float *s1, const float *s3, const float *s2,
@@ -310,13 +352,13 @@ void oracle_expert_ffn_q(int d, int F, int act, int wdtype, int bdtype, const do
     for (int f = 0; f < F; ++f) {
         double g = 0.0;
         for (int i = 0; i < d; ++i)
-            g += xv[i] * orc_load(W1, (size_t)f * d + i, wdtype);
+            g += xv[i] * orc_load_w(W1, (size_t)f, i, d, wdtype);
         if (s1)
             g *= (double)s1[f];
         if (act == ORC_SWIGLU) {
             double u = 0.0;
             for (int i = 0; i < d; ++i)
-                u += xv[i] * orc_load(W3, (size_t)f * d + i, wdtype);
+                u += xv[i] * orc_load_w(W3, (size_t)f, i, d, wdtype);
             if (s3)
                 u *= (double)s3[f];
             h[f] = g / (1.0 + exp(-g)) * u;
@@ -329,7 +371,7 @@ void oracle_expert_ffn_q(int d, int F, int act, int wdtype, int bdtype, const do
     for (int j = 0; j < d; ++j) {
         double o = 0.0;
         for (int f = 0; f < F; ++f)
-            o += h[f] * orc_load(W2, (size_t)j * F + f, wdtype);
+            o += h[f] * orc_load_w(W2, (size_t)j, f, F, wdtype);
         if (s2)
             o *= (double)s2[j];
         if (b2)
@@ -350,7 +392,7 @@ typedef struct {
     int d, F, E, k, act, dtype, wdtype;
     const void *x;
     const void *W1, *W3, *W2, *b1, *b2; /* [E,F,d], [E,F,d], [E,d,F], [E,F], [E,d] */
-    const float *s1, *s3, *s2;          /* E4M3 row scales [E,F], [E,F], [E,d] or NULL */
+    const float *s1, *s3, *s2;          /* low-bit row scales [E,F], [E,F], [E,d] or NULL */
     int F_sh;
     const void *S1, *S3, *S2; /* shared expert [F_sh,d], [F_sh,d], [d,F_sh] */
     const int *topk_idx;
@@ -385,13 +427,13 @@ static void orc_layer_range(void *p, long lo, long hi)
                 continue;
             }
             int e = c->topk_idx[a];
-            size_t wo = (size_t)e * F * d;
-            size_t we = c->wdtype == ORC_F32 ? 4 : c->wdtype == ORC_BF16 ? 2 : 1;
+            size_t up = (size_t)e * F * orc_row_bytes(d, c->wdtype);   /* W1, W3: F rows of d */
+            size_t dn = (size_t)e * d * orc_row_bytes(F, c->wdtype);   /* W2: d rows of F */
             size_t be = c->dtype == ORC_F32 ? 4 : 2;
             oracle_expert_ffn_q(d, F, c->act, c->wdtype, c->dtype, xv,
-                                (const char *)c->W1 + wo * we,
-                                c->W3 ? (const char *)c->W3 + wo * we : NULL,
-                                (const char *)c->W2 + wo * we,
+                                (const char *)c->W1 + up,
+                                c->W3 ? (const char *)c->W3 + up : NULL,
+                                (const char *)c->W2 + dn,
                                 c->b1 ? (const char *)c->b1 + (size_t)e * F * be : NULL,
                                 c->b2 ? (const char *)c->b2 + (size_t)e * d * be : NULL,
                                 c->s1 ? c->s1 + (size_t)e * F : NULL,

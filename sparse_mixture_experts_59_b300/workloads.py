@@ -204,3 +204,81 @@ def dequantize_experts_fp8(inp: dict) -> dict:
         if inp.get(key) is not None:
             out[key] = inp[key].float() * inp[skey][..., None]
     return out
+
+
+FP4_MAX = 6.0       # largest E2M1 magnitude
+FP4_CHUNK = 128     # values per packed chunk: 64 code bytes + 8 E4M3 block scales + 8 zero bytes
+FP4_CHUNK_BYTES = 80
+
+
+def _e2m1_round(q: torch.Tensor) -> torch.Tensor:
+    """E2M1 codes (sign bit 3, magnitude index 0..7 for 0, .5, 1, 1.5, 2, 3,
+    4, 6) of q, |q| <= 6, rounded to nearest with ties to the even mantissa."""
+    a = q.abs()
+    idx = ((a > 0.25).to(torch.uint8) + (a >= 0.75).to(torch.uint8) + (a > 1.25).to(torch.uint8)
+           + (a >= 1.75).to(torch.uint8) + (a > 2.5).to(torch.uint8) + (a >= 3.5).to(torch.uint8)
+           + (a > 5.0).to(torch.uint8))
+    return idx | ((q < 0).to(torch.uint8) << 3)
+
+
+def quantize_rows_fp4(w: torch.Tensor):
+    """One [R, K] weight matrix (K a multiple of 128) -> (packed uint8
+    [R, K/128 * 80], row scales fp32 [R]).  Row scale s = max|row| / (6*448);
+    block scale b (E4M3, per 16 values) = E4M3(max|block| / (6 s)), rounded to
+    nearest even; code = E2M1(w / (b s)) saturated to +-6.  Stored value of an
+    element: code * b, times s."""
+    R, K = w.shape
+    assert K % FP4_CHUNK == 0, "4-bit weights need rows of a multiple of 128 values"
+    wf = w.float()
+    rs = wf.abs().amax(dim=1) / (FP4_MAX * FP8_MAX)
+    rs = torch.where(rs > 0, rs, torch.ones_like(rs))
+    wb = wf.view(R, K // 16, 16)
+    bs_code = (wb.abs().amax(dim=2) / (FP4_MAX * rs[:, None])).to(torch.float8_e4m3fn)
+    denom = bs_code.float() * rs[:, None]
+    q = torch.where(denom[..., None] > 0, wb / denom[..., None], torch.zeros_like(wb))
+    codes = _e2m1_round(q.clamp(-FP4_MAX, FP4_MAX)).view(R, K // FP4_CHUNK, FP4_CHUNK)
+    packed = torch.zeros(R, K // FP4_CHUNK, FP4_CHUNK_BYTES, dtype=torch.uint8, device=w.device)
+    packed[:, :, :64] = codes[:, :, 0::2] | (codes[:, :, 1::2] << 4)
+    packed[:, :, 64:72] = bs_code.view(torch.uint8).view(R, K // FP4_CHUNK, 8)
+    return packed.view(R, -1), rs
+
+
+def quantize_experts_fp4(inp: dict) -> dict:
+    """Copy of a workload whose routed expert weights W1, W3, W2 are packed
+    4-bit weights (E2M1 codes with E4M3 scales per 16 values, see
+    quantize_rows_fp4) with one fp32 scale per output row (s1, s3 [E,F],
+    s2 [E,d]).  Sets cfg['weight_fp4'].  Input preparation only."""
+    out = dict(inp)
+    cfg = dict(inp["cfg"])
+    cfg["weight_fp4"] = True
+    out["cfg"] = cfg
+    for key, skey in (("W1", "s1"), ("W3", "s3"), ("W2", "s2")):
+        w = inp.get(key)
+        if w is None:
+            out[key] = None
+            out[skey] = None
+            continue
+        E, R, K = w.shape
+        packed = torch.empty(E, R, K // FP4_CHUNK * FP4_CHUNK_BYTES, dtype=torch.uint8,
+                             device=w.device)
+        scales = torch.empty(E, R, dtype=torch.float32, device=w.device)
+        for e in range(E):                   # one expert at a time bounds the fp32 temporaries
+            packed[e], scales[e] = quantize_rows_fp4(w[e])
+        out[key] = packed
+        out[skey] = scales
+    return out
+
+
+def dequantize_rows_fp4(packed: torch.Tensor, rs: torch.Tensor) -> torch.Tensor:
+    """float64 [R, K] of a packed 4-bit matrix: code value * block scale * row
+    scale, each factor exact in float64."""
+    R = packed.shape[0]
+    chunks = packed.view(R, -1, FP4_CHUNK_BYTES).to(torch.int64)
+    lo, hi = chunks[:, :, :64] & 15, chunks[:, :, :64] >> 4
+    codes = torch.stack([lo, hi], dim=3).view(R, -1, FP4_CHUNK)
+    mag = torch.tensor([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], dtype=torch.float64,
+                       device=packed.device)
+    vals = mag[codes & 7] * torch.where(codes >= 8, -1.0, 1.0).to(torch.float64)
+    bs = chunks[:, :, 64:72].to(torch.uint8).contiguous().view(torch.float8_e4m3fn).double()
+    vals = vals.view(R, -1, 8, 16) * bs[..., None]
+    return vals.view(R, -1) * rs.double()[:, None]

@@ -464,3 +464,54 @@ def test_fp8_expert_layer_equals_dequantised_fp64_layer():
             h = g * expit(g) * u
             ref += routed["topk_w"][t, s] * (deq("W2", "s2") @ h)
         np.testing.assert_allclose(routed["y"][r], ref, rtol=1e-12, atol=1e-12)
+
+
+# ----------------------------------------------------- 4-bit expert weights
+def test_e2m1_decoding_matches_the_format_value_set():
+    """E2M1 (1 sign, 2 exponent, 1 mantissa bit) has the eight magnitudes
+    0, 0.5, 1, 1.5, 2, 3, 4, 6 on codes 0..7 and their negatives on 8..15 (the
+    OCP microscaling format's value table); the oracle decodes its codes from
+    the bit fields."""
+    table = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    got = [oracle.e2m1_value(c) for c in range(16)]
+    assert got[:8] == table
+    assert got[8:] == [-v for v in table]
+    assert np.signbit(got[8])                    # code 8 is -0
+
+
+def test_fp4_quantiser_error_bound():
+    """Every element of a 4-bit matrix decodes to within one block-scale step of
+    the weight it came from: |w - q b s| <= b s (the largest E2M1 gap is 2,
+    between 4 and 6), plus the saturation of |w| / (b s) above 6 when the
+    block scale rounded down."""
+    torch.manual_seed(3)
+    w = (torch.randn(7, 384) * 0.02).to(torch.bfloat16)
+    packed, rs = workloads.quantize_rows_fp4(w)
+    deq = workloads.dequantize_rows_fp4(packed, rs)
+    bs = packed.view(7, -1, 80)[:, :, 64:72].contiguous().view(torch.float8_e4m3fn).double()
+    step = (bs * rs.double()[:, None, None]).repeat_interleave(16, dim=2).view(7, -1)
+    excess = (w.double().abs() - 6.0 * step).clamp(min=0)
+    assert torch.all((deq - w.double()).abs() <= step + excess + 1e-30)
+    assert torch.all(packed.view(7, -1, 80)[:, :, 72:] == 0)
+
+
+def test_fp4_expert_layer_equals_dequantised_fp64_layer():
+    """A layer with packed 4-bit expert weights and row scales equals the same
+    layer on the weights decoded by an independent (torch) decoder of the
+    packed layout, computed with numpy in float64."""
+    inp = workloads.make_inputs(workloads.config("mixtral_prefill", T=5, d=128, F=256, E=3, k=2,
+                                                 seed=43))
+    q = workloads.quantize_experts_fp4(inp)
+    tokens = np.arange(5)
+    routed = oracle.layer_forward(q, tokens=tokens)
+    xf = inp["x"].double().numpy()
+    deq = lambda key, skey, e: workloads.dequantize_rows_fp4(q[key][e], q[skey][e]).numpy()
+    for r, t in enumerate(tokens):
+        ref = xf[t].copy()
+        for s in range(2):
+            e = routed["topk_idx"][t, s]
+            g = deq("W1", "s1", e) @ xf[t]
+            u = deq("W3", "s3", e) @ xf[t]
+            h = g * expit(g) * u
+            ref += routed["topk_w"][t, s] * (deq("W2", "s2", e) @ h)
+        np.testing.assert_allclose(routed["y"][r], ref, rtol=1e-12, atol=1e-12)
