@@ -55,6 +55,8 @@ def parse_args():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--fp8", action="store_true",
                     help="the main workload with FP8 E4M3 expert weights (profiling cases)")
+    ap.add_argument("--fp4", action="store_true",
+                    help="the main workload with packed 4-bit (E2M1) expert weights")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--sweep", default=None,
                     help="comma-separated token counts: time the layer at each T on the "
@@ -276,11 +278,11 @@ def run_ours(args, world, rank, local):
     cfg = workload_config(args)
     inp = workloads.make_inputs(cfg, device=dev)
     bf16_inp = inp
-    if args.fp8:
-        inp = workloads.quantize_experts_fp8(inp)
+    if args.fp8 or args.fp4:
+        inp = (workloads.quantize_experts_fp4 if args.fp4 else workloads.quantize_experts_fp8)(inp)
         cfg = inp["cfg"]
         if args.no_decode:
-            bf16_inp = None                      # only the FP8 copy stays on the device
+            bf16_inp = None                      # only the low-bit copy stays on the device
     layer = binding.MoeLayer(cfg, inp, device=dev)
     x = inp["x"]
     outputs = {"y": torch.empty_like(x), "counts_kept": torch.empty(cfg["E"], dtype=torch.int32,
@@ -313,7 +315,8 @@ def run_ours(args, world, rank, local):
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16, e4m3 expert weights" if args.fp8 else "bf16",
+        "dtype": ("bf16, e2m1 expert weights" if args.fp4 else
+                  "bf16, e4m3 expert weights" if args.fp8 else "bf16"),
         "data": "synthetic: seeded x~N(0,1), expert weights~N(0,0.02), router~N(0,1/sqrt(d)); bf16",
         "config": {"workload": args.workload, "T": cfg["T"], "d_model": cfg["d"], "d_ff": cfg["F"],
                    "experts": cfg["E"], "top_k": cfg["k"], "act": cfg["act"],
@@ -340,7 +343,8 @@ def run_ours(args, world, rank, local):
         result["e2e"] = run_e2e(layer, cfg, x, args, world, dev)
     if not args.no_decode:
         result["decode"] = run_decode(args, bf16_inp, world, dev, peaks, peak_src)
-        result["decode_fp8"] = run_decode(args, bf16_inp, world, dev, peaks, peak_src, fp8=True)
+        result["decode_fp8"] = run_decode(args, bf16_inp, world, dev, peaks, peak_src, low="fp8")
+        result["decode_fp4"] = run_decode(args, bf16_inp, world, dev, peaks, peak_src, low="fp4")
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(inp, cfg, args.cpu_seconds)
     del layer
@@ -404,16 +408,20 @@ def run_e2e(layer, cfg, x, args, world, dev):
                                        "overlap the layer of step i (double-buffered, own streams)"}
 
 
-def run_decode(args, prefill_inp, world, dev, peaks, peak_src, fp8=False):
+def run_decode(args, prefill_inp, world, dev, peaks, peak_src, low=None):
     """Decode-shaped layer (T=32) on the same expert weights: weight streaming
-    of the experts that got tokens, against the HBM roofline.  fp8=True: the
-    same weights quantised to E4M3 with per-row scales (half the bytes)."""
+    of the experts that got tokens, against the HBM roofline.  low="fp8": the
+    same weights quantised to E4M3 with per-row scales (half the bytes);
+    low="fp4": packed 4-bit (80 bytes per 128 values, 0.3125 of the bytes)."""
     cfg = workloads.config(args.decode_workload)
     inp = dict(prefill_inp)
     inp["x"] = workloads.make_x(cfg, dev)
     inp["cfg"] = cfg
-    if fp8:
+    if low == "fp8":
         inp = workloads.quantize_experts_fp8(inp)
+        cfg = inp["cfg"]
+    elif low == "fp4":
+        inp = workloads.quantize_experts_fp4(inp)
         cfg = inp["cfg"]
     layer = binding.MoeLayer(cfg, inp, device=dev)
     outputs = {"y": torch.empty_like(inp["x"]),
@@ -423,13 +431,18 @@ def run_decode(args, prefill_inp, world, dev, peaks, peak_src, fp8=False):
     ms = max_over_ranks(ms, world)
     counts = outputs["counts_kept"].cpu().numpy()
     hit = int((counts > 0).sum())
-    per_expert = 3 * cfg["d"] * cfg["F"] * (1 if fp8 else 2) + (2 * cfg["F"] + cfg["d"]) * 4 * fp8
+    # weight bytes per routed expert: codes (+ block scales) + fp32 row scales
+    code_bytes = {None: 2.0, "fp8": 1.0, "fp4": 80.0 / 128.0}[low]
+    per_expert = int(3 * cfg["d"] * cfg["F"] * code_bytes) + \
+        (2 * cfg["F"] + cfg["d"]) * 4 * (low is not None)
     wbytes = hit * per_expert
     gemm_s = (stages["up_gemm"] + stages["down_gemm"]) / 1e3
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     gbs = wbytes / gemm_s / 1e9
     del layer
-    return {"workload": args.decode_workload + (" (FP8 E4M3 expert weights)" if fp8 else ""),
+    tag = {None: "", "fp8": " (FP8 E4M3 expert weights)",
+           "fp4": " (packed 4-bit E2M1 expert weights, E4M3 block scales)"}[low]
+    return {"workload": args.decode_workload + tag,
             "T": cfg["T"], "experts_hit": hit,
             "tokens_per_s": round(cfg["T"] * world / (ms / 1e3), 1), "ms_per_step": round(ms, 4),
             "weight_bytes": wbytes, "gemm_ms": round(gemm_s * 1e3, 4),

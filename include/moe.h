@@ -98,6 +98,14 @@ enum moe_scoring { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 };
  *           row i of W1 is s1[i] * W1[i,:] ("How Mixture of Experts Works",
  *           "Quantization for MoE").  bf16 layers without a shared expert;
  *           d and F multiples of 16.
+ *  weight_fp4 0 (default); 1: routed expert weights are packed 4-bit weights
+ *           (not with weight_fp8): each row of K values (K = d for W1, W3; F
+ *           for W2; a multiple of 128) is K/128 chunks of 80 bytes -- 64 bytes
+ *           of E2M1 codes (value 2i of the chunk in the low nibble of byte i,
+ *           value 2i+1 in the high nibble), 8 E4M3 scales (scale b multiplies
+ *           values 16b .. 16b+15), 8 zero bytes -- with the fp32 row scales
+ *           s1, s3, s2 on top: w = code * block scale * row scale.  bf16
+ *           layers without a shared expert; d and F multiples of 128.
  * A zero-filled moe_cfg with the sizes set gives the pages' default router. */
 typedef struct moe_cfg {
     int T, d, F, E, k;
@@ -109,11 +117,12 @@ typedef struct moe_cfg {
     int scoring;
     int no_renorm;
     int weight_fp8;
+    int weight_fp4;
 } moe_cfg;
 
 /* Expert weights (device pointers, dtype of the layer).  W3 only for SwiGLU;
  * b1, b2 only with has_bias; S1, S3, S2 only with F_shared > 0; s1 [E,F],
- * s3 [E,F], s2 [E,d] (fp32 row scales) only with weight_fp8. */
+ * s3 [E,F], s2 [E,d] (fp32 row scales) only with weight_fp8 or weight_fp4. */
 typedef struct moe_weights {
     const void *W1, *W3, *W2;
     const void *b1, *b2;

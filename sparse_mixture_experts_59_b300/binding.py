@@ -37,7 +37,8 @@ class MoeConfig(ctypes.Structure):
                 ("E", ctypes.c_int), ("k", ctypes.c_int), ("F_shared", ctypes.c_int),
                 ("dtype", ctypes.c_int), ("act", ctypes.c_int), ("has_bias", ctypes.c_int),
                 ("capacity_factor", ctypes.c_float), ("scoring", ctypes.c_int),
-                ("no_renorm", ctypes.c_int), ("weight_fp8", ctypes.c_int)]
+                ("no_renorm", ctypes.c_int), ("weight_fp8", ctypes.c_int),
+                ("weight_fp4", ctypes.c_int)]
 
 
 WEIGHT_KEYS = ("W1", "W3", "W2", "b1", "b2", "S1", "S3", "S2", "s1", "s3", "s2")
@@ -104,7 +105,8 @@ def make_config(cfg: dict) -> MoeConfig:
         capacity_factor=float(cfg.get("capacity_factor", 0.0) or 0.0),
         scoring=MOE_SCORE_SIGMOID if cfg.get("scoring", "softmax") == "sigmoid" else MOE_SCORE_SOFTMAX,
         no_renorm=0 if cfg.get("renorm", True) else 1,
-        weight_fp8=int(bool(cfg.get("weight_fp8", False))))
+        weight_fp8=int(bool(cfg.get("weight_fp8", False))),
+        weight_fp4=int(bool(cfg.get("weight_fp4", False))))
 
 
 def _p(t):

@@ -57,7 +57,7 @@ Layout layout_of(const moe_cfg& c) {
     auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes); return at; };
     L.ctrl = take(kCtrlWords * 4);
     L.tile_status = take((size_t)dispatch_blocks((int)A) * E * 4);
-    L.split_ticket = take(c.weight_fp8 ? (size_t)kFp8SplitTickets * 4 : 0);
+    L.split_ticket = take(c.weight_fp8 || c.weight_fp4 ? (size_t)kFp8SplitTickets * 4 : 0);
     L.rank = take(A * 4);
     L.prob_part = take((size_t)router_blocks(c.T) * E * 4);
     L.prob_mean = take(E * 4);
@@ -79,7 +79,7 @@ Layout layout_of(const moe_cfg& c) {
     L.hsh = take(T * (size_t)c.F_shared * es);
     L.ys = take(A * c.d * es);
     L.sh = take(c.F_shared > 0 ? T * c.d * es : 0);
-    L.split_part = take(c.weight_fp8 ? fp8_split_bytes(c) : 0);
+    L.split_part = take(c.weight_fp8 || c.weight_fp4 ? fp8_split_bytes(c) : 0);
     L.total = o;
     return L;
 }
@@ -108,6 +108,12 @@ int check_cfg(const moe_cfg* c) {
     if (c->weight_fp8 != 0 && c->weight_fp8 != 1) return fail(MOE_ERR_INVALID_ARG, "weight_fp8 must be 0 or 1%s");
     if (c->weight_fp8 && (c->dtype != MOE_BF16 || c->F_shared > 0))
         return fail(MOE_ERR_UNSUPPORTED, "FP8 expert weights need a bf16 layer without a shared expert%s");
+    if (c->weight_fp4 != 0 && c->weight_fp4 != 1) return fail(MOE_ERR_INVALID_ARG, "weight_fp4 must be 0 or 1%s");
+    if (c->weight_fp4 && c->weight_fp8) return fail(MOE_ERR_INVALID_ARG, "weight_fp4 and weight_fp8 exclude each other%s");
+    if (c->weight_fp4 && (c->dtype != MOE_BF16 || c->F_shared > 0))
+        return fail(MOE_ERR_UNSUPPORTED, "4-bit expert weights need a bf16 layer without a shared expert%s");
+    if (c->weight_fp4 && (c->d % 128 || c->F % 128))
+        return fail(MOE_ERR_INVALID_ARG, "4-bit expert weights need d and F multiples of 128 (80-byte chunks)%s");
     if (c->weight_fp8 && (c->d % 16 || c->F % 16))
         return fail(MOE_ERR_INVALID_ARG, "FP8 expert weights need d and F multiples of 16 (16-byte rows)%s");
     return MOE_OK;
@@ -158,7 +164,7 @@ int check_weights(const moe_cfg& c, const moe_weights* w) {
         MOE_TRY(check_ptr(w->S3, "S3"));
         MOE_TRY(check_ptr(w->S2, "S2"));
     }
-    if (c.weight_fp8) {
+    if (c.weight_fp8 || c.weight_fp4) {
         MOE_TRY(check_ptr4(w->s1, "s1"));
         MOE_TRY(check_ptr4(w->s2, "s2"));
         if (c.act == MOE_SWIGLU) MOE_TRY(check_ptr4(w->s3, "s3"));
@@ -209,11 +215,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // Row-major [rows, cols] matrix of 2-byte elements (bf16, or f16 with
 // dt = CU_TENSOR_MAP_DATA_TYPE_FLOAT16); box = box_rows rows x 64 columns
 // (128 bytes), 128-byte swizzle, out-of-range elements read as zero.
-// 1-byte elements (E4M3 weights, dt = UINT8): 64-byte box rows, no swizzle.
+// 1-byte elements (low-bit weights, dt = UINT8): box_cols bytes per box row;
+// swizzle = false leaves the box rows packed (packed 4-bit weights).
 int encode_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, const char* what,
                 uint32_t box_rows = 128,
                 CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                uint32_t box_cols = 64) {
+                uint32_t box_cols = 64, bool swizzle = true) {
     auto fn = encode_fn();
     if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled unavailable%s");
     if (rows == 0) rows = 1;
@@ -223,7 +230,8 @@ int encode_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, 
     const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "tensor map encode failed for %s", what);
     return MOE_OK;
@@ -316,9 +324,18 @@ int run_expert_ffn(const moe_cfg& c, const DevInfo& di, const void* x, const int
     void* H = at<char>(ws, L.h);
     void* Hsh = at<char>(ws, L.hsh);
     const int rows_sh = c.F_shared > 0 ? c.T : 0;
-    if (c.weight_fp8) {
+    if (c.weight_fp8 || c.weight_fp4) {
         if (di.cc != 103)
-            return fail(MOE_ERR_UNSUPPORTED, "FP8 expert GEMMs need an sm_103a (B300) device%s");
+            return fail(MOE_ERR_UNSUPPORTED, "low-bit expert GEMMs need an sm_103a (B300) device%s");
+        const bool fp4 = c.weight_fp4 != 0;
+        // E4M3: rows of K bytes, 128-byte boxes, swizzled; packed E2M1: rows of
+        // K/128 * 80 bytes, 80-byte boxes, not swizzled
+        auto wmap = [&](CUtensorMap* m, const void* base, uint64_t rows, int K, const char* what) {
+            return fp4 ? encode_rows(m, base, rows, (uint64_t)(K / 128) * 80, what, 64,
+                                     CU_TENSOR_MAP_DATA_TYPE_UINT8, 80, false)
+                       : encode_rows(m, base, rows, (uint64_t)K, what, 64,
+                                     CU_TENSOR_MAP_DATA_TYPE_UINT8, 128);
+        };
         const int up_mode = c.act == MOE_SWIGLU ? kModeSwiglu : kModeGelu;
         MOE_CUDA(launch_gather_f16(x, perm_src, offsets, c.E, c.k, c.T, c.d, Xp, status,
                                    di.num_sms, st),
@@ -327,10 +344,8 @@ int run_expert_ffn(const moe_cfg& c, const DevInfo& di, const void* x, const int
         CUtensorMap maps[3];
         MOE_TRY(encode_rows(&maps[0], Xp, (uint64_t)A, c.d, "gathered rows", 16,
                             CU_TENSOR_MAP_DATA_TYPE_FLOAT16));
-        MOE_TRY(encode_rows(&maps[1], w.W1, (uint64_t)c.E * c.F, c.d, "W1", 64,
-                            CU_TENSOR_MAP_DATA_TYPE_UINT8, 128));
-        MOE_TRY(encode_rows(&maps[2], c.act == MOE_SWIGLU ? w.W3 : w.W1, (uint64_t)c.E * c.F, c.d,
-                            "W3", 64, CU_TENSOR_MAP_DATA_TYPE_UINT8, 128));
+        MOE_TRY(wmap(&maps[1], w.W1, (uint64_t)c.E * c.F, c.d, "W1"));
+        MOE_TRY(wmap(&maps[2], c.act == MOE_SWIGLU ? w.W3 : w.W1, (uint64_t)c.E * c.F, c.d, "W3"));
         int* tickets = at<int>(ws, L.split_ticket);
         float* part = at<float>(ws, L.split_part);
         const long long part_bytes = (long long)fp8_split_bytes(c);
@@ -343,12 +358,11 @@ int run_expert_ffn(const moe_cfg& c, const DevInfo& di, const void* x, const int
         up.status = status;
         up.wscale = w.s1;
         up.wscale2 = c.act == MOE_SWIGLU ? w.s3 : nullptr;
-        MOE_CUDA(launch_ffn_fp8(up_mode, maps, up, di.num_sms, st), "up-projection launch");
+        MOE_CUDA(launch_ffn_fp8(up_mode, maps, up, di.num_sms, st, fp4), "up-projection launch");
         if (ev) MOE_CUDA(cudaEventRecord(ev[1], st), "event record");
         MOE_TRY(encode_rows(&maps[0], H, (uint64_t)A, c.F, "hidden rows", 16,
                             CU_TENSOR_MAP_DATA_TYPE_FLOAT16));
-        MOE_TRY(encode_rows(&maps[1], w.W2, (uint64_t)c.E * c.d, c.F, "W2", 64,
-                            CU_TENSOR_MAP_DATA_TYPE_UINT8, 128));
+        MOE_TRY(wmap(&maps[1], w.W2, (uint64_t)c.E * c.d, c.F, "W2"));
         maps[2] = maps[1];
         TcFfnArgs dn{};
         dn.split_ticket = tickets; dn.split_tickets = kFp8SplitTickets;
@@ -359,7 +373,8 @@ int run_expert_ffn(const moe_cfg& c, const DevInfo& di, const void* x, const int
         dn.perm_src = perm_src; dn.gate_w = topk_w;
         dn.status = status;
         dn.wscale = w.s2;
-        MOE_CUDA(launch_ffn_fp8(kModeDown, maps, dn, di.num_sms, st), "down-projection launch");
+        MOE_CUDA(launch_ffn_fp8(kModeDown, maps, dn, di.num_sms, st, fp4),
+                 "down-projection launch");
         if (ev) MOE_CUDA(cudaEventRecord(ev[2], st), "event record");
         return MOE_OK;
     }

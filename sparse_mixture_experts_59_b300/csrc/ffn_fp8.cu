@@ -1,10 +1,13 @@
-// ffn_fp8.cu -- grouped expert GEMMs with FP8 (E4M3) expert weights.
+// ffn_fp8.cu -- grouped expert GEMMs with low-bit expert weights: FP8 (E4M3)
+// codes, or packed 4-bit (E2M1) codes with E4M3 block scales.
 //
 // The low-bit-weights variant of the expert FFNs: expert weights are stored
-// as E4M3 codes q with one fp32 scale per output row, w = q * s, which halves
-// the bytes that cross HBM -- the bound of decode-sized batches ("How Mixture
-// of Experts Works", "Quantization for MoE": quantised expert weights).  The
-// maths is that of ffn_tc.cu on the dequantised weights:
+// as codes q with one fp32 scale per output row, w = q * s (for 4-bit codes
+// q = code * block scale, one block scale per 16 values), which halves (E4M3)
+// or cuts to 0.31 (packed E2M1) the bytes that cross HBM -- the bound of
+// decode-sized batches ("How Mixture of Experts Works", "Quantization for
+// MoE": quantised expert weights).  The maths is that of ffn_tc.cu on the
+// dequantised weights:
 //   SwiGLU  H = silu(s1 (A q1^T)) * (s3 (A q3^T))
 //   GELU    H = gelu(s1 (A q1^T) + b1)
 //   down    Ys[perm_src[r]] = topk_w * (s2 (H q2^T) + b2)
@@ -26,20 +29,23 @@
 // MMA read), which at 128 B/clock caps the weight stream near the HBM rate;
 // through TMEM it is 2 bytes.
 //
-// One CTA per SM, 384 threads; the warps that issue TMA or MMA instructions
+// One CTA per SM, 384 threads (512 for 4-bit weights, which have two
+// converter warps per lane quadrant); the warps that issue TMA or MMA instructions
 // sit on different schedulers (warp % 4), as issuing them slows the other
 // warps of the scheduler (measured: a converter warp sharing its scheduler
 // with two MMA issuers ran ~2400 clocks behind one sharing with none, and the
 // slowest converter gates both the weight ring and the MMAs):
-//   warp 0      TMA: E4M3 weight rows (128 bytes of K, 128-byte swizzle) into
-//               a 10-stage ring that the converters release as soon as they
-//               hold a stage's codes in registers;
+//   warp 0      TMA: weight rows (E4M3: 128 bytes of K, 128-byte swizzle,
+//               10-stage ring; E2M1: 80 bytes, 16 stages) into a ring that
+//               the converters release as soon as they hold a stage's codes
+//               in registers;
 //   warp 1      TMEM owner; TMA: the tile's f16 token rows (128-byte swizzle)
 //               in chunks of up to 24 KB into two buffers, a chunk ahead;
-//   warps 6-9   converters, one per TMEM lane quadrant, thread = weight row:
-//               E4M3 -> f16 pairs in registers, tcgen05.st into the TMEM A
-//               buffer of the stage's block;
-//   warps 10-11 MMA issuers, issuer i for blocks i and i + 2 of the tile:
+//   warps 6-9   converters (6-13 for 4-bit), one (two) per TMEM lane
+//               quadrant, thread = weight row: codes -> f16 pairs in
+//               registers, tcgen05.st into the TMEM A buffer of the stage's
+//               block;
+//   last two    MMA issuers, issuer i for blocks i and i + 2 of the tile:
 //               tcgen05.mma kind::f16 (M=128, N=tokens, K=16), A from the
 //               block's TMEM buffer, B (tokens) from shared memory, into the
 //               block's accumulator.  A thread issues a small MMA only every
@@ -77,45 +83,60 @@ namespace moe {
 
 namespace {
 
-constexpr int BK = 128;                        // K per stage: one 128-byte row of codes
+constexpr int BK = 128;                        // K values per stage
 constexpr int WROWS = 128;                     // weight rows per block (MMA M, TMEM lanes)
 constexpr int G = 4;                           // weight blocks per tile
 constexpr int NISS = 2;                        // MMA issuers, blocks i, i + NISS, ...
 constexpr int TOK = 32;                        // tokens per tile at most (MMA N)
 constexpr int TOK_BOX = 16;                    // token rows per TMA box
-constexpr int WSTAGES = 10;                    // E4M3 weight ring
 constexpr int TB_BYTES = 24 * 1024;            // token chunk buffer (two of them)
-constexpr int WQ_BYTES = WROWS * BK;           // E4M3 codes of one stage
 constexpr int A_COLS = BK / 2;                 // TMEM columns of one A buffer (f16 pairs)
 constexpr int ACC_SET = G * TOK;               // TMEM columns of a tile's accumulators
 constexpr int A_COL0 = 2 * ACC_SET;            // two accumulator sets, then the A buffers
 constexpr int TMEM_COLS = 512;
 static_assert(A_COL0 + G * A_COLS <= TMEM_COLS, "tensor memory budget (an A buffer per block)");
-constexpr int CVT_WARPS = 4;                   // 4 or 8: one or two per TMEM lane quadrant
-constexpr int CVT_CHUNKS = 8 / (CVT_WARPS / 4);  // 16-code chunks per converter thread and stage
-static_assert(CVT_WARPS == 4 || CVT_WARPS == 8, "converter warps cover each lane quadrant");
 constexpr int TOKP_WARP = 1;                   // token producer (and TMEM owner)
-constexpr int MMA_WARP0 = 6 + CVT_WARPS;       // first MMA issuer
-constexpr int NUM_THREADS = (MMA_WARP0 + NISS) * 32;
-static_assert(MMA_WARP0 % 4 == 2 && NISS == 2, "issuers on schedulers 2 and 3");
 constexpr int XCH_LD = 33;
 
-constexpr int OFF_TOK = 0;
-constexpr int OFF_WQ = OFF_TOK + 2 * TB_BYTES;
-constexpr int OFF_XCH = OFF_WQ + WSTAGES * WQ_BYTES;
-constexpr int OFF_PRE = OFF_XCH + 64 * XCH_LD * 4;   // [2][G][128] row scales, biases
-constexpr int OFF_TOKA = OFF_PRE + 2 * G * WROWS * 4;
-constexpr int OFF_TOKW = OFF_TOKA + 2 * TOK * 4;     // token slots and weights, 2 buffers
-constexpr int OFF_BAR = OFF_TOKW + 2 * TOK * 4;
-constexpr int NUM_BARS = 2 * WSTAGES + 2 + 2 + 2 * G + 2 + 2 + NISS;
-constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-constexpr int OFF_START = OFF_MISC + 32;
-constexpr int OFF_OFFS = OFF_START + (kMaxExperts + 2) * 4;
-constexpr int SMEM_USED = OFF_OFFS + (kMaxExperts + 2) * 4;
-constexpr int SMEM_BYTES = SMEM_USED + 1024;
-static_assert(OFF_TOK % 1024 == 0 && TB_BYTES % 1024 == 0, "swizzled token atoms");
-static_assert(OFF_WQ % 1024 == 0 && WQ_BYTES % 1024 == 0, "swizzled weight stages");
-static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+// Weight formats.  Both give a stage 128 values of each weight row (one MMA K
+// range of 128): E4M3 rows of 128 bytes (128-byte swizzle), or packed E2M1
+// rows of 80 bytes (64 code bytes, 8 E4M3 block scales, 8 zero bytes; 80-byte
+// rows put the 16-byte pieces of 8 consecutive rows in 8 different bank
+// groups without a swizzle).  The 4-bit conversion does twice the work per
+// stage (a cvt and a block-scale multiply per pair), so it has two converter
+// warps per TMEM lane quadrant; its ring has more, smaller stages for the same
+// bytes in flight.
+enum { kFmtE4M3 = 0, kFmtE2M1 = 1 };
+template <int FMT>
+struct WF {
+    static constexpr int ROW_BYTES = FMT == kFmtE4M3 ? 128 : 80;
+    static constexpr int WQ_BYTES = WROWS * ROW_BYTES;          // one stage of weight rows
+    static constexpr int WSTAGES = FMT == kFmtE4M3 ? 10 : 16;   // weight ring
+    static constexpr int CVT_WARPS = FMT == kFmtE4M3 ? 4 : 8;   // one or two per lane quadrant
+    static constexpr int MMA_WARP0 = 6 + CVT_WARPS;             // first MMA issuer
+    static constexpr int NUM_THREADS = (MMA_WARP0 + NISS) * 32;
+    static constexpr int OFF_TOK = 0;
+    static constexpr int OFF_WQ = OFF_TOK + 2 * TB_BYTES;
+    static constexpr int OFF_XCH = OFF_WQ + WSTAGES * WQ_BYTES;
+    static constexpr int OFF_PRE = OFF_XCH + 64 * XCH_LD * 4;   // [2][G][128] row scales, biases
+    static constexpr int OFF_TOKA = OFF_PRE + 2 * G * WROWS * 4;
+    static constexpr int OFF_TOKW = OFF_TOKA + 2 * TOK * 4;     // token slots and weights, 2 buffers
+    static constexpr int OFF_BAR = OFF_TOKW + 2 * TOK * 4;
+    static constexpr int NUM_BARS = 2 * WSTAGES + 2 + 2 + 2 * G + 2 + 2 + NISS;
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+    static constexpr int OFF_START = OFF_MISC + 32;
+    static constexpr int OFF_OFFS = OFF_START + (kMaxExperts + 2) * 4;
+    static constexpr int SMEM_USED = OFF_OFFS + (kMaxExperts + 2) * 4;
+    static constexpr int SMEM_BYTES = SMEM_USED + 1024;
+    static_assert(MMA_WARP0 % 4 == 2 && NISS == 2, "issuers on schedulers 2 and 3");
+    static_assert(OFF_TOK % 1024 == 0 && TB_BYTES % 1024 == 0, "swizzled token atoms");
+    static_assert(OFF_WQ % 1024 == 0 && (FMT != kFmtE4M3 || WQ_BYTES % 1024 == 0),
+                  "swizzled weight stages");
+    static_assert(WQ_BYTES % 256 == 0, "128-byte aligned weight boxes");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+};
+template struct WF<kFmtE4M3>;
+template struct WF<kFmtE2M1>;
 
 template <int MODE>
 struct Fp8Traits {
@@ -256,49 +277,50 @@ __device__ __forceinline__ void finish_block(const TcFfnArgs& p, const Seg& t, i
     }
 }
 
-template <int MODE>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+template <int MODE, int FMT>
+__global__ void __launch_bounds__(WF<FMT>::NUM_THREADS, 1)
 ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__ CUtensorMap mapW,
                const __grid_constant__ CUtensorMap mapW3, const TcFfnArgs p) {
+    using F = WF<FMT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t* sTok = smem + OFF_TOK;
-    uint8_t* sWq = smem + OFF_WQ;
-    float* s_xch = reinterpret_cast<float*>(smem + OFF_XCH);
-    float* s_pre = reinterpret_cast<float*>(smem + OFF_PRE);
-    int* s_tok_a = reinterpret_cast<int*>(smem + OFF_TOKA);
-    float* s_tok_w = reinterpret_cast<float*>(smem + OFF_TOKW);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+    uint8_t* sTok = smem + F::OFF_TOK;
+    uint8_t* sWq = smem + F::OFF_WQ;
+    float* s_xch = reinterpret_cast<float*>(smem + F::OFF_XCH);
+    float* s_pre = reinterpret_cast<float*>(smem + F::OFF_PRE);
+    int* s_tok_a = reinterpret_cast<int*>(smem + F::OFF_TOKA);
+    float* s_tok_w = reinterpret_cast<float*>(smem + F::OFF_TOKW);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + F::OFF_BAR);
     uint64_t* wfull = bars;                      // E4M3 codes landed
-    uint64_t* wempty = wfull + WSTAGES;          // converters hold the codes
-    uint64_t* kfull = wempty + WSTAGES;          // a token chunk landed
+    uint64_t* wempty = wfull + F::WSTAGES;          // converters hold the codes
+    uint64_t* kfull = wempty + F::WSTAGES;          // a token chunk landed
     uint64_t* kempty = kfull + 2;                // the issuers done with the chunk
     uint64_t* cfull = kempty + 2;                // converted weights in block j's A buffer
     uint64_t* cempty = cfull + G;                // block j's MMAs done with it
     uint64_t* tfull = cempty + G;                // the issuers' accumulators complete
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;                // per issuer
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
-    volatile int* s_abort = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
-    volatile int* s_go = reinterpret_cast<volatile int*>(smem + OFF_MISC + 8);
-    volatile int* s_last = reinterpret_cast<volatile int*>(smem + OFF_MISC + 12);
-    int* s_maxrows = reinterpret_cast<int*>(smem + OFF_MISC + 16);
-    int* s_start = reinterpret_cast<int*>(smem + OFF_START);
-    int* s_off = reinterpret_cast<int*>(smem + OFF_OFFS);
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + F::OFF_MISC);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(smem + F::OFF_MISC + 4);
+    volatile int* s_go = reinterpret_cast<volatile int*>(smem + F::OFF_MISC + 8);
+    volatile int* s_last = reinterpret_cast<volatile int*>(smem + F::OFF_MISC + 12);
+    int* s_maxrows = reinterpret_cast<int*>(smem + F::OFF_MISC + 16);
+    int* s_start = reinterpret_cast<int*>(smem + F::OFF_START);
+    int* s_off = reinterpret_cast<int*>(smem + F::OFF_OFFS);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < WSTAGES; ++s) {
+        for (int s = 0; s < F::WSTAGES; ++s) {
             ptx::mbar_init(&wfull[s], 1);
-            ptx::mbar_init(&wempty[s], CVT_WARPS);
+            ptx::mbar_init(&wempty[s], F::CVT_WARPS);
         }
         for (int s = 0; s < 2; ++s) {
             ptx::mbar_init(&kfull[s], 1);
             ptx::mbar_init(&kempty[s], NISS);
         }
         for (int b = 0; b < G; ++b) {
-            ptx::mbar_init(&cfull[b], CVT_WARPS);
+            ptx::mbar_init(&cfull[b], F::CVT_WARPS);
             ptx::mbar_init(&cempty[b], 1);
         }
         for (int a = 0; a < 2; ++a) {
@@ -324,7 +346,7 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
     // partial-sum scratch, which the two projections share, is first touched
     // by the epilogue, after MMAs that consumed waited-for tokens.
     pdl_trigger();
-    for (int i = threadIdx.x; i <= p.E; i += NUM_THREADS) s_off[i] = p.offsets[i];
+    for (int i = threadIdx.x; i <= p.E; i += F::NUM_THREADS) s_off[i] = p.offsets[i];
     __syncthreads();
     const int nwb = (p.N + Fp8Traits<MODE>::UNITS - 1) / Fp8Traits<MODE>::UNITS;
     if (warp == 0) {            // longest segment: sizes the token chunks
@@ -394,14 +416,14 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
             FOR_EACH_SEG(t)
                 for (int kb = t.kb0; ok && kb < t.kb1; ++kb)
                     for (int j = 0; j < t.nblk; ++j, ++it) {
-                        const int s = it % WSTAGES;
-                        const uint32_t ph = (uint32_t)(it / WSTAGES) & 1u;
+                        const int s = it % F::WSTAGES;
+                        const uint32_t ph = (uint32_t)(it / F::WSTAGES) & 1u;
                         if (!ptx::mbar_wait(&wempty[s], ph ^ 1u, s_abort)) { ok = false; break; }
-                        ptx::mbar_arrive_expect_tx(&wfull[s], WQ_BYTES);
+                        ptx::mbar_arrive_expect_tx(&wfull[s], F::WQ_BYTES);
                         const int2 wr = block_rows<MODE>(p, t, j);
-                        uint8_t* wq = sWq + s * WQ_BYTES;
-                        ptx::tma_load_2d(wq, &mapW, &wfull[s], kb * BK, wr.x);
-                        ptx::tma_load_2d(wq + WQ_BYTES / 2, &mapW3, &wfull[s], kb * BK, wr.y);
+                        uint8_t* wq = sWq + s * F::WQ_BYTES;
+                        ptx::tma_load_2d(wq, &mapW, &wfull[s], kb * F::ROW_BYTES, wr.x);
+                        ptx::tma_load_2d(wq + F::WQ_BYTES / 2, &mapW3, &wfull[s], kb * F::ROW_BYTES, wr.y);
                     }
                 if (!ok) break;
             }
@@ -409,8 +431,8 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
                 *s_abort = 1;
                 raise_error(p.status, MOE_ERR_DEVICE_TIMEOUT);
             }
-            for (int j = (it > WSTAGES ? it - WSTAGES : 0); j < it; ++j)
-                ptx::mbar_wait(&wfull[j % WSTAGES], (uint32_t)(j / WSTAGES) & 1u, nullptr);
+            for (int j = (it > F::WSTAGES ? it - F::WSTAGES : 0); j < it; ++j)
+                ptx::mbar_wait(&wfull[j % F::WSTAGES], (uint32_t)(j / F::WSTAGES) & 1u, nullptr);
         }
     } else if (warp == TOKP_WARP) {
         // ----------------------------------- TMA producer (token chunks)
@@ -447,13 +469,13 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
             for (int j = (cc > 2 ? cc - 2 : 0); j < cc; ++j)
                 ptx::mbar_wait(&kfull[j & 1], (uint32_t)(j >> 1) & 1u, nullptr);
         }
-    } else if (warp >= MMA_WARP0) {
+    } else if (warp >= F::MMA_WARP0) {
         // ------------------------------------------------------- MMA issuers
         // Issuer mi takes blocks mi, mi + NISS, ... of every tile (their A
         // buffers and accumulators).  An issuer without a block in a tile
         // still arrives on the tile's shared barriers (token chunks,
         // accumulators).
-        const int mi = warp - MMA_WARP0;
+        const int mi = warp - F::MMA_WARP0;
         if (lane == 0) {
             uint32_t nfill = 0;                 // bit j: parity of block j's fills so far
             int tc = 0, cc = 0;                 // tiles, token chunks
@@ -521,35 +543,52 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
         }
     } else if (warp >= 6) {
         // -------------------------------------------------------- converters
-        // Thread = weight row r (the warp's TMEM lane quadrant) and part h of
-        // the stage's K: chunks h*CVT_CHUNKS .. of 16 codes, read at their
-        // swizzled places (c ^ (r & 7)), so that 8 consecutive rows hit 8
-        // different bank groups; chunk c -> 8 f16 pairs -> TMEM columns 8c ..
-        // 8c+7 of the A buffer.
+        // Thread = weight row r of the warp's TMEM lane quadrant q and part h
+        // (one of CVT_WARPS / 4) of the stage's 128 values; the part's f16
+        // pairs go to TMEM columns (64 / parts) h .. of the block's A buffer.
+        //   E4M3: chunk c (16 codes) of the row sits at c ^ (r & 7) (128-byte
+        //   swizzle: 8 consecutive rows hit 8 different bank groups); a code
+        //   pair -> an f16 pair (exact).
+        //   E2M1: the row's 80 bytes hold 64 code bytes (values 2i, 2i+1 in the
+        //   low, high nibble of byte i) and 8 E4M3 scales, one per 16 values;
+        //   a code byte -> an f16 pair, times its block scale as an f16 pair
+        //   (exact: every E2M1 value times an E4M3 value is an f16 value).
+        constexpr int PARTS = F::CVT_WARPS / 4;
+        constexpr int COLS = 64 / PARTS;                     // TMEM columns per part
+        static_assert(FMT == kFmtE4M3 || PARTS == 2, "an E2M1 part is 4 pieces' worth of scales");
         const int q = warp & 3, h = (warp - 6) >> 2;
         const int r = q * 32 + lane;
         const uint32_t a_lane =
-            tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(A_COL0 + 8 * h * CVT_CHUNKS);
+            tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(A_COL0 + COLS * h);
         int it = 0;
         uint32_t nfill = 0;                      // bit j: parity of A buffer j's fills so far
         bool ok = true;
         FOR_EACH_SEG(t)
             for (int kb = t.kb0; ok && kb < t.kb1; ++kb)
                 for (int j = 0; j < t.nblk; ++j, ++it) {
-                    const int s = it % WSTAGES, b = j;
-                    const uint32_t ph = (uint32_t)(it / WSTAGES) & 1u;
+                    const int s = it % F::WSTAGES, b = j;
+                    const uint32_t ph = (uint32_t)(it / F::WSTAGES) & 1u;
                     const uint32_t bph = (nfill >> b) & 1u;
                     nfill ^= 1u << b;
                     if (!__all_sync(0xffffffffu, ptx::mbar_wait(&wfull[s], ph, s_abort))) {
                         ok = false;
                         break;
                     }
-                    uint4 qv[CVT_CHUNKS];
-                    const uint8_t* src = sWq + s * WQ_BYTES + r * 128;
+                    const uint8_t* src = sWq + s * F::WQ_BYTES + r * F::ROW_BYTES;
+                    constexpr int NQ = FMT == kFmtE4M3 ? 8 / PARTS : 4 / PARTS;
+                    uint4 qv[NQ];
+                    uint32_t sc = 0;                             // E2M1: the part's block scales
+                    if constexpr (FMT == kFmtE4M3) {
 #pragma unroll
-                    for (int i = 0; i < CVT_CHUNKS; ++i)
-                        qv[i] = *reinterpret_cast<const uint4*>(
-                            src + (((CVT_CHUNKS * h + i) ^ (r & 7)) << 4));
+                        for (int i = 0; i < NQ; ++i)
+                            qv[i] = *reinterpret_cast<const uint4*>(
+                                src + (((NQ * h + i) ^ (r & 7)) << 4));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < NQ; ++i)
+                            qv[i] = *reinterpret_cast<const uint4*>(src + (NQ * h + i) * 16);
+                        sc = *reinterpret_cast<const uint32_t*>(src + 64 + 4 * h);
+                    }
                     __syncwarp();
                     if (lane == 0) ptx::mbar_arrive(&wempty[s]);     // codes are in registers
                     if (!__all_sync(0xffffffffu, ptx::mbar_wait(&cempty[b], bph ^ 1u, s_abort))) {
@@ -557,18 +596,43 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
                         break;
                     }
                     ptx::tc_fence_after();
+                    if constexpr (FMT == kFmtE4M3) {
 #pragma unroll
-                    for (int hh = 0; hh < CVT_CHUNKS / 2; ++hh) {   // 16 columns at a time
-                        uint32_t wv[16];
+                        for (int hh = 0; hh < NQ / 2; ++hh) {     // 16 columns at a time
+                            uint32_t wv[16];
 #pragma unroll
-                        for (int i = 0; i < 2; ++i) {
-                            const uint4 c = qv[2 * hh + i];
-                            e4m3x4_to_f16x4(c.x, wv[8 * i + 0], wv[8 * i + 1]);
-                            e4m3x4_to_f16x4(c.y, wv[8 * i + 2], wv[8 * i + 3]);
-                            e4m3x4_to_f16x4(c.z, wv[8 * i + 4], wv[8 * i + 5]);
-                            e4m3x4_to_f16x4(c.w, wv[8 * i + 6], wv[8 * i + 7]);
+                            for (int i = 0; i < 2; ++i) {
+                                const uint4 c = qv[2 * hh + i];
+                                e4m3x4_to_f16x4(c.x, wv[8 * i + 0], wv[8 * i + 1]);
+                                e4m3x4_to_f16x4(c.y, wv[8 * i + 2], wv[8 * i + 3]);
+                                e4m3x4_to_f16x4(c.z, wv[8 * i + 4], wv[8 * i + 5]);
+                                e4m3x4_to_f16x4(c.w, wv[8 * i + 6], wv[8 * i + 7]);
+                            }
+                            ptx::tmem_st16(a_lane + (uint32_t)(b * A_COLS + hh * 16), wv);
                         }
-                        ptx::tmem_st16(a_lane + (uint32_t)(b * A_COLS + hh * 16), wv);
+                    } else {
+                        // 16 bytes = 32 values = two blocks of 16 per piece
+                        const uint32_t s01 = ptx::cvt_e4m3x2_f16x2((uint16_t)(sc & 0xffffu));
+                        const uint32_t s23 = ptx::cvt_e4m3x2_f16x2((uint16_t)(sc >> 16));
+#pragma unroll
+                        for (int i = 0; i < NQ; ++i) {              // 16 columns per piece
+                            const uint32_t pair = i < 1 ? s01 : s23;
+                            const uint32_t b0 = __byte_perm(pair, 0, 0x1010);   // low half, twice
+                            const uint32_t b1 = __byte_perm(pair, 0, 0x3232);   // high half, twice
+                            const uint32_t words[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
+                            uint32_t wv[16];
+#pragma unroll
+                            for (int w = 0; w < 4; ++w) {
+                                const uint32_t bs = w < 2 ? b0 : b1;
+#pragma unroll
+                                for (int by = 0; by < 4; ++by)
+                                    wv[4 * w + by] = ptx::mul_f16x2(
+                                        ptx::cvt_e2m1x2_f16x2(
+                                            (uint16_t)((words[w] >> (8 * by)) & 0xffu)),
+                                        bs);
+                            }
+                            ptx::tmem_st16(a_lane + (uint32_t)(b * A_COLS + i * 16), wv);
+                        }
                     }
                     ptx::tc_fence_before();
                     __syncwarp();
@@ -687,16 +751,29 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
 
 }  // namespace
 
-cudaError_t launch_ffn_fp8(int mode, const CUtensorMap* maps, const TcFfnArgs& p, int num_sms,
-                           cudaStream_t st) {
-    auto kernel = mode == kModeSwiglu ? ffn_fp8_kernel<kModeSwiglu>
-                : mode == kModeGelu ? ffn_fp8_kernel<kModeGelu> : ffn_fp8_kernel<kModeDown>;
-    const cudaError_t err =
-        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+template <int MODE, int FMT>
+cudaError_t launch_one(const CUtensorMap* maps, const TcFfnArgs& p, int num_sms, cudaStream_t st) {
+    auto kernel = ffn_fp8_kernel<MODE, FMT>;
+    const cudaError_t err = cudaFuncSetAttribute(
+        kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, WF<FMT>::SMEM_BYTES);
     if (err != cudaSuccess) return err;
     const int grid = num_sms < kFp8MaxGrid ? num_sms : kFp8MaxGrid;
-    return launch_kernel(kernel, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, st, 1, maps[0],
-                         maps[1], maps[2], p);
+    return launch_kernel(kernel, dim3(grid), dim3(WF<FMT>::NUM_THREADS), WF<FMT>::SMEM_BYTES, st,
+                         1, maps[0], maps[1], maps[2], p);
+}
+
+template <int FMT>
+cudaError_t launch_fmt(int mode, const CUtensorMap* maps, const TcFfnArgs& p, int num_sms,
+                       cudaStream_t st) {
+    if (mode == kModeSwiglu) return launch_one<kModeSwiglu, FMT>(maps, p, num_sms, st);
+    if (mode == kModeGelu) return launch_one<kModeGelu, FMT>(maps, p, num_sms, st);
+    return launch_one<kModeDown, FMT>(maps, p, num_sms, st);
+}
+
+cudaError_t launch_ffn_fp8(int mode, const CUtensorMap* maps, const TcFfnArgs& p, int num_sms,
+                           cudaStream_t st, bool fp4) {
+    return fp4 ? launch_fmt<kFmtE2M1>(mode, maps, p, num_sms, st)
+               : launch_fmt<kFmtE4M3>(mode, maps, p, num_sms, st);
 }
 
 }  // namespace moe

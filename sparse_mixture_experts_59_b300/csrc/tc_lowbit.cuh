@@ -22,6 +22,23 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2_f16x2(uint16_t v) {
     return out;
 }
 
+// Two E2M1 floats (one byte: the low nibble first) -> two f16 packed in 32 bits
+// (low nibble in the low half); exact, as every E2M1 value is an f16 value.
+__device__ __forceinline__ uint32_t cvt_e2m1x2_f16x2(uint16_t byte) {
+    uint32_t out;
+    asm("{\n\t.reg .b8 b;\n\tcvt.u8.u16 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}"
+        : "=r"(out)
+        : "h"(byte));
+    return out;
+}
+
+// a * b for two f16 pairs (round to nearest even).
+__device__ __forceinline__ uint32_t mul_f16x2(uint32_t a, uint32_t b) {
+    uint32_t out;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(out) : "r"(a), "r"(b));
+    return out;
+}
+
 // Instruction descriptor, kind::f16 with f16 A/B (format 0), fp32 accumulator.
 __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
     return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
