@@ -57,6 +57,11 @@
 //               memory before its accumulators are ready: a global load waits
 //               several microseconds while the weight stream runs.
 //
+// The waits of the warps off the critical path (producers, issuers, epilogue)
+// sleep between polls: the converters that share their schedulers are the
+// bound, and polling takes issue slots from them (measured: 4% on the 4-bit
+// up-projection of a decode batch).
+//
 // Every E4M3 value (subnormals included, |v| <= 448) is an f16 value, so the
 // conversion (cvt.rn.f16x2.e4m3x2, two codes per instruction) is exact and the
 // products with the f16 tokens are exact in the fp32 accumulator.  (Measured:
@@ -418,7 +423,7 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
                     for (int j = 0; j < t.nblk; ++j, ++it) {
                         const int s = it % F::WSTAGES;
                         const uint32_t ph = (uint32_t)(it / F::WSTAGES) & 1u;
-                        if (!ptx::mbar_wait(&wempty[s], ph ^ 1u, s_abort)) { ok = false; break; }
+                        if (!ptx::mbar_wait_nap(&wempty[s], ph ^ 1u, s_abort, 64)) { ok = false; break; }
                         ptx::mbar_arrive_expect_tx(&wfull[s], F::WQ_BYTES);
                         const int2 wr = block_rows<MODE>(p, t, j);
                         uint8_t* wq = sWq + s * F::WQ_BYTES;
@@ -448,7 +453,7 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
                 for (int kc = t.kb0; kc < t.kb1; kc += CH, ++cc) {
                     const int kend = min(kc + CH, t.kb1);
                     const int ub = cc & 1;
-                    if (!ptx::mbar_wait(&kempty[ub], ((uint32_t)(cc >> 1) & 1u) ^ 1u, s_abort)) {
+                    if (!ptx::mbar_wait_nap(&kempty[ub], ((uint32_t)(cc >> 1) & 1u) ^ 1u, s_abort, 256)) {
                         ok = false;
                         break;
                     }
@@ -485,7 +490,7 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
                 const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
                 ++tc;
                 const bool mine = mi < t.nblk;
-                if (!ptx::mbar_wait(&tempty[acc], aph ^ 1u, s_abort)) { ok = false; break; }
+                if (!ptx::mbar_wait_nap(&tempty[acc], aph ^ 1u, s_abort, 64)) { ok = false; break; }
                 ptx::tc_fence_after();
                 const uint32_t idesc = ptx::idesc_f16_f32(WROWS, t.nmma);
                 const int atom = t.nmma * 128;
@@ -493,7 +498,7 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
                 int kc = t.kb0;
                 for (int kb = t.kb0; ok && kb < t.kb1; ++kb) {
                     if ((kb - t.kb0) % CH == 0) {                // next token chunk
-                        if (!ptx::mbar_wait(&kfull[cc & 1], (uint32_t)(cc >> 1) & 1u, s_abort)) {
+                        if (!ptx::mbar_wait_nap(&kfull[cc & 1], (uint32_t)(cc >> 1) & 1u, s_abort, 64)) {
                             ok = false;
                             break;
                         }
@@ -505,7 +510,7 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
                         ptx::sw128_desc(ptx::smem_u32(tb + (2 * (kb - kc) + 1) * atom));
                     const uint32_t first = kb > t.kb0 ? 1u : 0u;
                     for (int j = mi; j < t.nblk; j += NISS) {
-                        if (!ptx::mbar_wait(&cfull[j], (nfill >> j) & 1u, s_abort)) {
+                        if (!ptx::mbar_wait_nap(&cfull[j], (nfill >> j) & 1u, s_abort, 64)) {
                             ok = false;
                             break;
                         }
@@ -634,6 +639,7 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
                             ptx::tmem_st16(a_lane + (uint32_t)(b * A_COLS + i * 16), wv);
                         }
                     }
+                    ptx::tmem_wait_st();                  // the stage's stores, then signal
                     ptx::tc_fence_before();
                     __syncwarp();
                     if (lane == 0) ptx::mbar_arrive(&cfull[b]);
@@ -667,7 +673,7 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
                 }
             }
             int ok = 1;
-            if (lane == 0) ok = ptx::mbar_wait(&tfull[acc], aph, s_abort) ? 1 : 0;
+            if (lane == 0) ok = ptx::mbar_wait_nap(&tfull[acc], aph, s_abort, 512) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
             // the four epilogue warps share named barriers below, so they take
             // one decision: a snapshot of the abort flag between two barriers

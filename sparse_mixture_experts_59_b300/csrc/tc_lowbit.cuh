@@ -14,6 +14,22 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// mbar_wait for a warp whose wait is off the critical path: it sleeps `ns`
+// between polls, so that its polling takes no issue slots from the warps that
+// share its scheduler.  Same bounds as mbar_wait (abort flag, cycle limit).
+__device__ __forceinline__ bool mbar_wait_nap(uint64_t* bar, uint32_t parity,
+                                              const volatile int* abort_flag, unsigned ns) {
+    const uint32_t addr = smem_u32(bar);
+    if (mbar_try_wait(addr, parity)) return true;
+    const long long t0 = clock64();
+    while (true) {
+        __nanosleep(ns);
+        if (mbar_try_wait(addr, parity)) return true;
+        if (abort_flag && *abort_flag) return false;
+        if (clock64() - t0 > kWaitLimitCycles) return false;
+    }
+}
+
 // Two E4M3 floats (low byte first) -> two f16 packed in 32 bits; exact, as
 // every E4M3 value is an f16 value.
 __device__ __forceinline__ uint32_t cvt_e4m3x2_f16x2(uint16_t v) {
@@ -62,12 +78,15 @@ __device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem,
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};\n\t"
-        "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
         "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
         "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
         "r"(v[15])
         : "memory");
+}
+// Wait until this thread's earlier tcgen05.st have completed.
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 }  // namespace ptx
