@@ -629,12 +629,11 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
 #pragma unroll
                             for (int w = 0; w < 4; ++w) {
                                 const uint32_t bs = w < 2 ? b0 : b1;
+                                uint32_t c[4];
+                                ptx::cvt_e2m1x8_f16x8(words[w], c);
 #pragma unroll
                                 for (int by = 0; by < 4; ++by)
-                                    wv[4 * w + by] = ptx::mul_f16x2(
-                                        ptx::cvt_e2m1x2_f16x2(
-                                            (uint16_t)((words[w] >> (8 * by)) & 0xffu)),
-                                        bs);
+                                    wv[4 * w + by] = ptx::mul_f16x2(c[by], bs);
                             }
                             ptx::tmem_st16(a_lane + (uint32_t)(b * A_COLS + i * 16), wv);
                         }
