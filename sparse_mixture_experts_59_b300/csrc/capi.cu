@@ -42,7 +42,7 @@ int router_blocks(int T) {
 struct Layout {
     size_t ctrl, tile_status, split_ticket, rank, prob_part, prob_mean, router_part, logits, topk_idx, topk_w,
         counts_pre, counts_kept, offsets, perm_src, dest, drop_mask, stats, xp, h, hsh, ys, sh,
-        split_part, total;
+        split_part, front_part, total;
 };
 
 // FP8 expert GEMMs: tickets and fp32 partial sums of the tiles that straddle
@@ -80,6 +80,8 @@ Layout layout_of(const moe_cfg& c) {
     L.ys = take(A * c.d * es);
     L.sh = take(c.F_shared > 0 ? T * c.d * es : 0);
     L.split_part = take(c.weight_fp8 || c.weight_fp4 ? fp8_split_bytes(c) : 0);
+    const FrontSmallPlan fp = front_small_plan(c.T, c.d, c.E, c.k);
+    L.front_part = take(fp.ok ? (size_t)fp.splits * T * E * 4 : 0);
     L.total = o;
     return L;
 }
@@ -237,6 +239,13 @@ int encode_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, 
     return MOE_OK;
 }
 
+// Decode-sized batches route and dispatch in one launch (front_small.cu);
+// MOE_SMALL_FRONT=0 keeps the separate router and dispatch kernels.
+bool small_front_enabled() {
+    const char* env = getenv("MOE_SMALL_FRONT");
+    return !(env && env[0] == '0');
+}
+
 // Kernel for the bf16 expert GEMMs:
 //   kGemmTc1   1-SM kernel, tokens on M in 128-row tiles (ffn_tc.cu)
 //   kGemmPair  2-SM kernel, tokens on M in 256-row tiles (ffn_tc2.cu)
@@ -272,6 +281,23 @@ int run_route(const moe_cfg& c, const DevInfo& di, const void* x, const void* Wr
               const float* bias, float* logits, int* topk_idx, float* topk_w, float* prob_mean,
               void* ws, cudaStream_t st) {
     const Layout L = layout_of(c);
+    const FrontSmallPlan fp = front_small_plan(c.T, c.d, c.E, c.k);
+    if (fp.ok && small_front_enabled()) {
+        // decode-sized batch: the route part of the one-launch front, so that
+        // this call and the layer call give the same logits
+        FrontSmallArgs a{};
+        a.x = x; a.Wr = Wr; a.bias = bias;
+        a.T = c.T; a.d = c.d; a.E = c.E; a.k = c.k;
+        a.scoring = c.scoring; a.renorm = !c.no_renorm;
+        a.dispatch = 0;
+        a.cap = moe_capacity(&c);
+        a.ks = fp.ks; a.splits = fp.splits;
+        a.part = at<float>(ws, L.front_part);
+        a.ticket = at<int>(ws, L.ctrl) + kCtrlFrontDone;
+        a.logits = logits; a.topk_idx = topk_idx; a.topk_w = topk_w; a.prob_mean = prob_mean;
+        MOE_CUDA(launch_front_small(c.dtype, a, st), "router launch");
+        return MOE_OK;
+    }
     const float* part = logits;
     int nsplit = 1;
     const float* topk_bias = nullptr;
@@ -651,10 +677,30 @@ static int layer_forward_impl(const moe_cfg* cfg, const void* x, const void* Wr,
     void* Sh = c.F_shared > 0 ? at<char>(ws, L.sh) : nullptr;
     cudaEvent_t const* ev = reinterpret_cast<cudaEvent_t const*>(events);
     if (ev) MOE_CUDA(cudaEventRecord(ev[0], st), "event record");
-    MOE_TRY(run_route(c, di, x, Wr, logit_bias, logits, topk_idx, topk_w, prob_mean, ws, st));
-    if (ev) MOE_CUDA(cudaEventRecord(ev[1], st), "event record");
-    MOE_TRY(run_dispatch(c, di, topk_idx, prob_mean, counts_pre, counts_kept, offsets, perm_src,
-                         dest, drop, stats, ws, st));
+    const FrontSmallPlan fp = front_small_plan(c.T, c.d, c.E, c.k);
+    if (fp.ok && small_front_enabled()) {
+        // decode-sized batch: route + dispatch in one launch (the stage
+        // events after it coincide: the dispatch stage reads as zero)
+        FrontSmallArgs a{};
+        a.x = x; a.Wr = Wr; a.bias = logit_bias;
+        a.T = c.T; a.d = c.d; a.E = c.E; a.k = c.k;
+        a.scoring = c.scoring; a.renorm = !c.no_renorm;
+        a.dispatch = 1;
+        a.cap = moe_capacity(&c);
+        a.ks = fp.ks; a.splits = fp.splits;
+        a.part = at<float>(ws, L.front_part);
+        a.ticket = at<int>(ws, L.ctrl) + kCtrlFrontDone;
+        a.logits = logits; a.topk_idx = topk_idx; a.topk_w = topk_w; a.prob_mean = prob_mean;
+        a.counts_pre = counts_pre; a.counts_kept = counts_kept; a.offsets = offsets;
+        a.perm_src = perm_src; a.dest = dest; a.drop_mask = drop; a.stats = stats;
+        MOE_CUDA(launch_front_small(c.dtype, a, st), "route + dispatch launch");
+        if (ev) MOE_CUDA(cudaEventRecord(ev[1], st), "event record");
+    } else {
+        MOE_TRY(run_route(c, di, x, Wr, logit_bias, logits, topk_idx, topk_w, prob_mean, ws, st));
+        if (ev) MOE_CUDA(cudaEventRecord(ev[1], st), "event record");
+        MOE_TRY(run_dispatch(c, di, topk_idx, prob_mean, counts_pre, counts_kept, offsets,
+                             perm_src, dest, drop, stats, ws, st));
+    }
     if (ev) MOE_CUDA(cudaEventRecord(ev[2], st), "event record");
     MOE_TRY(run_expert_ffn(c, di, x, perm_src, offsets, topk_w, *w, Ys, Sh, ws, st,
                            ev ? ev + 3 : nullptr));

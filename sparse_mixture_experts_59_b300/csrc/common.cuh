@@ -20,6 +20,7 @@ enum CtrlWord {
     kCtrlDispatchDone = 2,
     kCtrlRouterDone = 3,
     kCtrlHoldBlock = 4,     // test hook: look-back block (id + 1) that never publishes
+    kCtrlFrontDone = 5,     // decode-sized route + dispatch: CTAs done with phase 1
     kCtrlWords = 64
 };
 

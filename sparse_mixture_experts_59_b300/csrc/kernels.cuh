@@ -25,6 +25,42 @@ cudaError_t launch_router_logits_simt(int dtype, const void* x, const void* Wr, 
                                       float* logits, int T, int d, int E, cudaStream_t st);
 // top-k reads nsplit partial-logit slabs part[s][T][E], adds them in order
 // and the bias, writes logits, then softmax / top-k / renormalise.
+// Decode-sized route + dispatch in one launch (front_small.cu): router GEMM
+// partials over K-slices, then the last CTA routes and dispatches.
+constexpr int kFrontMaxT = 256;       // tokens
+constexpr int kFrontMaxE = 256;       // experts
+constexpr int kFrontMaxA = 512;       // assignments T*k
+constexpr int kFrontMaxTE = 2048;     // router outputs T*E
+struct FrontSmallPlan {
+    bool ok;       // the shape fits the one-launch path
+    int ks;        // K values per CTA slice (a multiple of 32)
+    int splits;    // CTAs = K-slices (<= 32)
+};
+FrontSmallPlan front_small_plan(int T, int d, int E, int k);
+struct FrontSmallArgs {
+    const void* x;            // [T, d] (dtype of the layer)
+    const void* Wr;           // [E, d]
+    const float* bias;        // [E] logit bias or nullptr
+    int T, d, E, k, scoring, renorm;
+    int dispatch;             // 0: route only (the dispatch outputs untouched)
+    long long cap;            // capacity, < 0 = dropless
+    int ks, splits;
+    float* part;              // [splits][T][E] scratch
+    int* ticket;              // zero between calls
+    float* logits;            // [T, E]
+    int* topk_idx;            // [T, k]
+    float* topk_w;            // [T, k]
+    float* prob_mean;         // [E] or nullptr (route only)
+    int* counts_pre;          // [E]
+    int* counts_kept;         // [E]
+    int* offsets;             // [E + 1]
+    int* perm_src;            // [T*k] (first R entries written)
+    int* dest;                // [T*k]
+    unsigned char* drop_mask; // [T*k]
+    float* stats;             // [2]: aux loss, dropped fraction
+};
+cudaError_t launch_front_small(int dtype, const FrontSmallArgs& a, cudaStream_t st);
+
 cudaError_t launch_router_topk(const float* part, int nsplit, const float* bias, float* logits,
                                int T, int E, int k, int scoring, int renorm, int* topk_idx,
                                float* topk_w,

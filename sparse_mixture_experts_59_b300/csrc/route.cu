@@ -11,6 +11,7 @@
 #include "common.cuh"
 #include "kernels.cuh"
 #include "launch.cuh"
+#include "topk_warp.cuh"
 
 namespace moe {
 
@@ -121,67 +122,18 @@ router_topk_kernel(const float* part, int nsplit, const float* __restrict__ bias
                 l[j] = -INFINITY;
             }
         }
-        float m = l[0];
-#pragma unroll
-        for (int j = 1; j < VPL; ++j) m = fmaxf(m, l[j]);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        // ex: exp(l - max) (softmax) or the sigmoid score itself; p = ex * inv
-        float ex[VPL];
-        float z = 0.f;
-#pragma unroll
-        for (int j = 0; j < VPL; ++j) {
-            const bool ok = lane + 32 * j < E;
-            ex[j] = !ok ? 0.f
-                  : scoring == MOE_SCORE_SIGMOID ? 1.f / (1.f + expf(-l[j])) : expf(l[j] - m);
-            z += ex[j];
-        }
-        float inv = 1.f;
-        if (scoring != MOE_SCORE_SIGMOID) {
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-            inv = 1.f / z;
-        }
+        float ex[VPL], inv;
+        int my_idx;
+        float my_w;
+        route_token_warp<VPL>(l, E, k, scoring, renorm, lane, ex, inv, my_idx, my_w);
         if (want_p) {
 #pragma unroll
             for (int j = 0; j < VPL; ++j)
                 if (lane + 32 * j < E) s_psum[warp][lane + 32 * j] += ex[j] * inv;
         }
-        // top-k by repeated warp arg-max over the logits; (value desc, index asc)
-        unsigned taken = 0;       // bit j: lane's value j already selected
-        float kept_ex = 0.f, my_ex = 0.f;
-        int my_idx = -1;
-        for (int s = 0; s < k; ++s) {
-            float bv = -INFINITY;
-            int bi = 0x7fffffff;
-#pragma unroll
-            for (int j = 0; j < VPL; ++j) {
-                const int e = lane + 32 * j;
-                if (e < E && !(taken & (1u << j)) && (l[j] > bv || bi == 0x7fffffff)) {
-                    bv = l[j];
-                    bi = e;
-                }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-                if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-            }
-            // owner marks it; everyone learns exp(l - m) of the winner
-            const int owner = bi & 31, jj = bi >> 5;
-            float wex = 0.f;
-#pragma unroll
-            for (int j = 0; j < VPL; ++j)
-                if (j == jj) wex = ex[j];
-            wex = __shfl_sync(0xffffffffu, wex, owner);
-            if (lane == owner) taken |= 1u << jj;
-            kept_ex += wex;
-            if (lane == s) { my_idx = bi; my_ex = wex; }
-        }
         if (lane < k) {
             topk_idx[(size_t)t * k + lane] = my_idx;
-            topk_w[(size_t)t * k + lane] = renorm ? my_ex / kept_ex : my_ex * inv;
+            topk_w[(size_t)t * k + lane] = my_w;
         }
     }
     if (!want_p) return;
