@@ -15,60 +15,58 @@
 
 namespace moe {
 
-// Xp[r] = x[perm_src[r] / k] for r < R = offsets[E] (read on the device).
-// One warp per row, 16-byte vectors.
+// Xp[r] = x[perm_src[r] / k] for r < R = offsets[E] (read on the device);
+// TO_F16 converts bf16 x to f16 on the way (the token operand of the
+// low-bit-weight expert GEMMs, whose MMAs take f16).  A row is spread over
+// tpr threads (tpr a power of two up to 256, the block holding 256 / tpr
+// rows), 16-byte vectors, each thread's loads issued together before its
+// stores: at decode sizes (a few dozen rows) every row is a block and the
+// gather costs one memory round trip instead of one per 32 vectors.
+template <bool TO_F16>
 __global__ void __launch_bounds__(256)
 gather_rows_kernel(const uint4* __restrict__ x, const int* __restrict__ perm_src,
                    const int* __restrict__ offsets, int E, int k, int Ttok, int vec_per_row,
-                   uint4* __restrict__ Xp, int* __restrict__ status) {
+                   int tpr, uint4* __restrict__ Xp, int* __restrict__ status) {
+    constexpr int U = 4;                     // vectors in flight per thread
     pdl_wait();
     pdl_trigger();
     const int R = offsets[E];
-    const int warps = (gridDim.x * blockDim.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < R; r += warps) {
+    const int rpb = blockDim.x / tpr;
+    const int slot = threadIdx.x / tpr, tl = threadIdx.x % tpr;
+    for (int r = blockIdx.x * rpb + slot; r < R; r += gridDim.x * rpb) {
         const int a = perm_src[r];
         const int t = a / k;
         if (a < 0 || t >= Ttok) {
-            if (lane == 0) raise_error(status, MOE_ERR_DEVICE_BOUNDS);
+            if (tl == 0) raise_error(status, MOE_ERR_DEVICE_BOUNDS);
             continue;
         }
         const uint4* src = x + (size_t)t * vec_per_row;
         uint4* dst = Xp + (size_t)r * vec_per_row;
-        for (int v = lane; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
-    }
-}
-
-// As gather_rows_kernel, converting bf16 x to f16 on the way (the token
-// operand of the FP8-weight expert GEMMs, whose MMAs take f16).
-__global__ void __launch_bounds__(256)
-gather_rows_f16_kernel(const uint4* __restrict__ x, const int* __restrict__ perm_src,
-                       const int* __restrict__ offsets, int E, int k, int Ttok, int vec_per_row,
-                       uint4* __restrict__ Xp, int* __restrict__ status) {
-    pdl_wait();
-    pdl_trigger();
-    const int R = offsets[E];
-    const int warps = (gridDim.x * blockDim.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < R; r += warps) {
-        const int a = perm_src[r];
-        const int t = a / k;
-        if (a < 0 || t >= Ttok) {
-            if (lane == 0) raise_error(status, MOE_ERR_DEVICE_BOUNDS);
-            continue;
-        }
-        const uint4* src = x + (size_t)t * vec_per_row;
-        uint4* dst = Xp + (size_t)r * vec_per_row;
-        for (int v = lane; v < vec_per_row; v += 32) {
-            float f[8];
-            unpack16(__ldg(src + v), f);
-            uint32_t w[4];
+        for (int v0 = tl; v0 < vec_per_row; v0 += U * tpr) {
+            uint4 q[U];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const __half2 h = __floats2half2_rn(f[2 * j], f[2 * j + 1]);
-                w[j] = *reinterpret_cast<const uint32_t*>(&h);
+            for (int u = 0; u < U; ++u) {
+                const int v = v0 + u * tpr;
+                if (v < vec_per_row) q[u] = __ldg(src + v);
             }
-            dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int v = v0 + u * tpr;
+                if (v >= vec_per_row) continue;
+                if constexpr (TO_F16) {
+                    float f[8];
+                    unpack16(q[u], f);
+                    uint32_t w[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const __half2 h = __floats2half2_rn(f[2 * j], f[2 * j + 1]);
+                        w[j] = *reinterpret_cast<const uint32_t*>(&h);
+                    }
+                    dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+                } else {
+                    dst[v] = q[u];
+                }
+            }
         }
     }
 }
@@ -119,28 +117,39 @@ combine_kernel(const T* __restrict__ x, const T* __restrict__ Ys,
     }
 }
 
+// threads per gathered row: the power of two >= vectors per row, 32..256
+static int gather_threads_per_row(int vpr) {
+    int t = 32;
+    while (t < 256 && t < vpr) t <<= 1;
+    return t;
+}
+// blocks of 256 threads for A rows (at most 16 per SM; the kernel loops)
+static unsigned gather_blocks(int A, int tpr, int num_sms) {
+    const int rpb = 256 / tpr;
+    long long blocks = ((long long)A + rpb - 1) / rpb;
+    if (blocks > num_sms * 16) blocks = num_sms * 16;
+    if (blocks < 1) blocks = 1;
+    return (unsigned)blocks;
+}
+
 cudaError_t launch_gather(int dtype, const void* x, const int* perm_src, const int* offsets, int E,
                           int k, int T, int d, void* Xp, int* status, int num_sms,
                           cudaStream_t st) {
     const int esize = dtype == MOE_F32 ? 4 : 2;
     const int vpr = d * esize / 16;
-    const int A = T * k;
-    long long blocks = ((long long)A * 32 + 255) / 256;
-    if (blocks > num_sms * 16) blocks = num_sms * 16;
-    if (blocks < 1) blocks = 1;
-    return launch_kernel(gather_rows_kernel, dim3((unsigned)blocks), dim3(256), 0, st, 1,
-                         (const uint4*)x, perm_src, offsets, E, k, T, vpr, (uint4*)Xp, status);
+    const int tpr = gather_threads_per_row(vpr);
+    return launch_kernel(gather_rows_kernel<false>, dim3(gather_blocks(T * k, tpr, num_sms)),
+                         dim3(256), 0, st, 1, (const uint4*)x, perm_src, offsets, E, k, T, vpr,
+                         tpr, (uint4*)Xp, status);
 }
 
 cudaError_t launch_gather_f16(const void* x, const int* perm_src, const int* offsets, int E, int k,
                               int T, int d, void* Xp, int* status, int num_sms, cudaStream_t st) {
     const int vpr = d * 2 / 16;
-    const int A = T * k;
-    long long blocks = ((long long)A * 32 + 255) / 256;
-    if (blocks > num_sms * 16) blocks = num_sms * 16;
-    if (blocks < 1) blocks = 1;
-    return launch_kernel(gather_rows_f16_kernel, dim3((unsigned)blocks), dim3(256), 0, st, 1,
-                         (const uint4*)x, perm_src, offsets, E, k, T, vpr, (uint4*)Xp, status);
+    const int tpr = gather_threads_per_row(vpr);
+    return launch_kernel(gather_rows_kernel<true>, dim3(gather_blocks(T * k, tpr, num_sms)),
+                         dim3(256), 0, st, 1, (const uint4*)x, perm_src, offsets, E, k, T, vpr,
+                         tpr, (uint4*)Xp, status);
 }
 
 cudaError_t launch_combine(int dtype, const void* x, const void* Ys, const unsigned char* drop_mask,
