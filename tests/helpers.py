@@ -38,6 +38,17 @@ SMALL = {
                                  renorm=False, capacity_factor=1.0, seed=2008),
     "sigmoid_fp32_norenorm": dict(base="tiny_fp32", T=90, scoring="sigmoid", renorm=False,
                                   seed=2009),
+    # decode-sized layers (T*k <= 512, T*E <= 2048): the one-launch route +
+    # dispatch, with 2, 8 and 4 router values per lane, k up to 8, a logit
+    # bias, capacity drops and d below one 128-wide K-slice
+    "decode_e64_k8": dict(base="fine_grained", T=32, d=256, F=128, E=64, k=8, F_shared=128,
+                          seed=2010),
+    "decode_e256_k8": dict(base="fine_grained", T=8, d=192, F=128, E=256, k=8, F_shared=128,
+                           seed=2011),
+    "decode_e128_sigmoid_cap": dict(base="mixtral_prefill", T=16, d=64, F=128, E=128, k=6,
+                                    scoring="sigmoid", renorm=False, capacity_factor=1.0,
+                                    seed=2012),
+    "decode_switch_bias": dict(base="switch_skewed", T=64, d=128, F=256, E=16, k=1, seed=2013),
 }
 
 
