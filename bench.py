@@ -33,7 +33,15 @@ from sparse_mixture_experts_59_b300 import binding, workloads  # noqa: E402
 
 METRIC = "MoE-layer tokens/s at Mixtral shape bf16; grouped-GEMM % BF16 peak; decode HBM GB/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
-KERNELS_PER_STEP = 8   # router logits, top-k, dispatch rank, dispatch scatter, gather, up, down, combine
+
+def kernels_per_step(cfg):
+    """The library's kernel launches for one layer call of `cfg`: a
+    decode-sized batch routes and dispatches in one launch (T <= 256,
+    T*k <= 512, T*E <= 2048), else router logits, top-k, dispatch rank and
+    dispatch scatter; then gather, up, down, combine."""
+    T, E, k = cfg["T"], cfg["E"], cfg["k"]
+    front = 1 if (T <= 256 and T * k <= 512 and T * E <= 2048) else 4
+    return front + 4
 
 
 def parse_args():
@@ -334,7 +342,7 @@ def run_ours(args, world, rank, local):
         "timing": "value from %d plain layer calls; stage_ms and the roofline's launch_ms from "
                   "%d more calls with CUDA events at the stage boundaries" % (args.steps, args.steps),
         "layer_tflops": round(alg["total"] / (ms / 1e3) / 1e12, 1),
-        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "gpu_launches": kernels_per_step(cfg) * args.steps,
         "pdl": os.environ.get("MOE_PDL", "1") != "0",
         "clocks": clk,
     }
