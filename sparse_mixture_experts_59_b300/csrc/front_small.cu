@@ -37,10 +37,10 @@ constexpr int kMaxOut = kFrontMaxTE / kThreads;    // partial outputs per thread
 constexpr int kMaxSplits = 32;
 constexpr int kRawBytes = 44 * 1024;
 
-// phase 1: [rows][kc + 1] fp32 chunks of x and Wr, kc a multiple of 32 sized
+// phase 1: [rows][kc + 4] fp32 chunks of x and Wr, kc a multiple of 32 sized
 // so that the T + E rows fit (T * E <= 2048 with T, E <= 256 bounds T + E by
 // 256 + 2048 / 256: kc >= 32 always; decode shapes take a K-slice in one chunk)
-static_assert((kFrontMaxT + kFrontMaxTE / kFrontMaxT) * 33 * 4 <= kRawBytes, "phase-1 shared memory");
+static_assert((kFrontMaxT + kFrontMaxTE / kFrontMaxT) * 36 * 4 <= kRawBytes, "phase-1 shared memory");
 // phase 2: logits, P_e partials, slots and ranks
 static_assert(2 * kFrontMaxTE * 4 + 2 * kFrontMaxA * 4 + 3 * kMaxExperts * 4 <= kRawBytes,
               "phase-2 shared memory");
@@ -67,9 +67,11 @@ front_small_kernel(const Tin* __restrict__ x, const Tin* __restrict__ Wr,
 
     // ---------------------------------------------- phase 1: partial logits
     {
-        int kcs = (kRawBytes / 4 / (Ttok + E) - 1) / 32 * 32;   // chunk (K values)
+        int kcs = (kRawBytes / 4 / (Ttok + E) - 4) / 32 * 32;   // chunk (K values)
         if (kcs > ks) kcs = ks;
-        const int ld = kcs + 1;                                 // padded rows
+        // rows padded by 4 floats: 16-byte aligned for float4 reads, and
+        // consecutive rows start 4 banks apart (conflict-free float4 reads)
+        const int ld = kcs + 4;
         float* xs = reinterpret_cast<float*>(s_raw);            // [Ttok][ld]
         float* ws = xs + Ttok * ld;                              // [E][ld]
         const int k0 = blockIdx.x * ks, k1 = min(d, k0 + ks);
@@ -112,10 +114,20 @@ front_small_kernel(const Tin* __restrict__ x, const Tin* __restrict__ Wr,
                 if (o < TE) {
                     const float* xr = xs + (o / E) * ld;
                     const float* wr = ws + (o % E) * ld;
-                    float s = acc[j];
-#pragma unroll 8
-                    for (int c = 0; c < kcs; ++c) s = fmaf(xr[c], wr[c], s);
-                    acc[j] = s;
+                    // four independent chains over float4 reads (kcs is a
+                    // multiple of 32), added in a fixed order
+                    const float4* x4 = reinterpret_cast<const float4*>(xr);
+                    const float4* w4 = reinterpret_cast<const float4*>(wr);
+                    float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+                    for (int c = 0; c < kcs / 4; ++c) {
+                        const float4 a = x4[c], b = w4[c];
+                        s4[0] = fmaf(a.x, b.x, s4[0]);
+                        s4[1] = fmaf(a.y, b.y, s4[1]);
+                        s4[2] = fmaf(a.z, b.z, s4[2]);
+                        s4[3] = fmaf(a.w, b.w, s4[3]);
+                    }
+                    acc[j] += (s4[0] + s4[1]) + (s4[2] + s4[3]);
                 }
             }
             __syncthreads();
@@ -191,8 +203,15 @@ front_small_kernel(const Tin* __restrict__ x, const Tin* __restrict__ Wr,
 
     // P_e (tokens added in order), then per-expert ranks in flattened order
     if (tid < E) {
-        float acc = 0.f;
-        for (int t = 0; t < Ttok; ++t) acc += s_prob[t * E + tid];
+        float a4[4] = {0.f, 0.f, 0.f, 0.f};      // four chains, fixed order
+        int t = 0;
+        for (; t + 4 <= Ttok; t += 4)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) a4[q] += s_prob[(t + q) * E + tid];
+#pragma unroll
+        for (int q = 0; q < 3; ++q)
+            if (t + q < Ttok) a4[q] += s_prob[(t + q) * E + tid];
+        const float acc = (a4[0] + a4[1]) + (a4[2] + a4[3]);
         s_pm[tid] = acc / (float)Ttok;
         if (prob_mean) prob_mean[tid] = s_pm[tid];
     }
