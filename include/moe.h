@@ -179,7 +179,13 @@ int moe_workspace_init(const moe_cfg *cfg, void *ws, size_t ws_bytes, void *stre
  *            (p[t,topk_idx[t,s]] itself with no_renorm)
  *   prob_mean[e] = mean over t of p[t,e]   (P_e of the aux loss; may be NULL)
  * x [T,d] and Wr [E,d] in the layer dtype; logit_bias [E] fp32 or NULL (a
- * fixed per-expert offset on the logits). */
+ * fixed per-expert offset on the logits).  The logits are fp32 sums of exact
+ * products; their summation order depends on the batch (decode-sized batches,
+ * T <= 256 with T*k <= 512 and T*E <= 2048, take K-sliced sums on CUDA cores;
+ * larger bf16 batches tensor-core tiles, larger fp32 ones a tiled CUDA-core
+ * GEMM), and moe_layer_forward uses the same order as this call, so both give
+ * the same bits.  MOE_SMALL_FRONT=0 in the environment takes the large-batch
+ * path at every size. */
 int moe_route(const moe_cfg *cfg, const void *x, const void *Wr, const float *logit_bias,
               float *logits, int *topk_idx, float *topk_w, float *prob_mean,
               void *ws, size_t ws_bytes, void *stream);
