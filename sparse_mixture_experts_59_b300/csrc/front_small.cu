@@ -5,7 +5,7 @@
 // Works", sections "The Gating Mechanism" and "The Capacity Factor", and the
 // MoELayer listing's flattened (token, slot) order; "Mixture-of-Experts
 // Routing", section "How a sparse MoE layer works": the first `capacity`
-// assignments in token order are kept).  At a few dozen tokens those five
+// assignments in token order are kept).  At a few dozen tokens those four
 // kernels are each a launch and a few dependent memory round trips with
 // almost no work, ~25 us together; here:
 //   every CTA  computes fp32 partial logits x[:, K-slice] . Wr[:, K-slice]^T
@@ -18,7 +18,7 @@
 //              in token order give the ranks, then capacity, offsets, dest /
 //              perm_src / drop mask and the aux loss.  It clears the ticket
 //              for the next call.
-// Measured at T=32 (Mixtral decode, ncu): five launches of 23 us together
+// Measured at T=32 (Mixtral decode, ncu): four launches of 23 us together
 // became one of ~11 us.
 // Used by the layer call when T*k <= 512 and T*E <= 2048 (T <= 256); the
 // router stage call uses the same kernel without the dispatch part, so both
