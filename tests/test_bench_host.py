@@ -1,0 +1,63 @@
+"""Host-side arithmetic of bench.py, on CPU: the algorithmic work its
+roofline divides by, and the kernel launches it claims per step.  The flop
+counts are checked against the workloads' published totals (the Mixtral
+prefill layer is 2.886e12 flop with its router; the fine-grained layer
+6.524e12) and against a count of multiply-adds written out per expert."""
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from sparse_mixture_experts_59_b300 import workloads  # noqa: E402
+
+
+def _macs_by_expert(cfg, rows_per_expert):
+    """Multiply-adds counted expert by expert: each kept row of an expert
+    multiplies d inputs by F outputs in the up projection (twice for SwiGLU's
+    gate and up), F by d in the down projection; the shared expert does the
+    same for all T tokens; the router d by E per token."""
+    d, F, E, T = cfg["d"], cfg["F"], cfg["E"], cfg["T"]
+    Fs = cfg.get("F_shared", 0) or 0
+    gates = 2 if cfg["act"] == "swiglu" else 1
+    up = sum(r * d * F * gates for r in rows_per_expert)
+    down = sum(r * F * d for r in rows_per_expert)
+    up += T * d * Fs * 2          # shared expert is SwiGLU
+    down += T * Fs * d
+    return up, down, T * d * E
+
+
+@pytest.mark.parametrize("name", ["mixtral_prefill", "mixtral_decode", "fine_grained",
+                                  "switch_skewed", "tiny_fp32"])
+def test_algorithmic_flops_are_twice_the_macs(name):
+    cfg = workloads.config(name)
+    A = cfg["T"] * cfg["k"]
+    rows = [A // cfg["E"]] * cfg["E"]          # any split of the kept rows
+    rows[0] += A - sum(rows)
+    up, down, router = _macs_by_expert(cfg, rows)
+    alg = bench.algorithmic(cfg, sum(rows))
+    assert alg["up"] == 2 * up
+    assert alg["down"] == 2 * down
+    assert alg["router"] == 2 * router
+    assert alg["total"] == 2 * (up + down + router)
+
+
+def test_published_totals():
+    """Mixtral prefill: 2.886e12 flop in the experts and router; the
+    fine-grained layer with its shared expert: 6.524e12."""
+    c1 = workloads.config("mixtral_prefill")
+    assert bench.algorithmic(c1, c1["T"] * c1["k"])["total"] == pytest.approx(2.886e12, rel=1e-3)
+    c3 = workloads.config("fine_grained")
+    assert bench.algorithmic(c3, c3["T"] * c3["k"])["total"] == pytest.approx(6.524e12, rel=1e-3)
+
+
+@pytest.mark.parametrize("name,launches", [("mixtral_prefill", 8), ("mixtral_decode", 5),
+                                           ("fine_grained", 8), ("switch_skewed", 8),
+                                           ("tiny_fp32", 5)])
+def test_kernel_launches_per_step(name, launches):
+    """Decode-sized batches route and dispatch in one launch; larger ones in
+    four.  Then gather, up, down, combine."""
+    assert bench.kernels_per_step(workloads.config(name)) == launches
