@@ -61,10 +61,11 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
-    ap.add_argument("--fp8", action="store_true",
-                    help="the main workload with FP8 E4M3 expert weights (profiling cases)")
-    ap.add_argument("--fp4", action="store_true",
-                    help="the main workload with packed 4-bit (E2M1) expert weights")
+    low = ap.add_mutually_exclusive_group()
+    low.add_argument("--fp8", action="store_true",
+                     help="the main workload with FP8 E4M3 expert weights (profiling cases)")
+    low.add_argument("--fp4", action="store_true",
+                     help="the main workload with packed 4-bit (E2M1) expert weights")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--sweep", default=None,
                     help="comma-separated token counts: time the layer at each T on the "
