@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import oracle
-from helpers import TOL_Y, f64, max_rel, moe_rel
+from helpers import TOL_AUX, TOL_Y, f64, max_rel, moe_rel
 from sparse_mixture_experts_59_b300 import binding, workloads
 
 pytestmark = pytest.mark.gpu
@@ -28,6 +28,19 @@ def _layer_vs_oracle(cfg, zero_router=False):
     assert max_rel(f64(out["y"]), ref["y"]) < TOL_Y[cfg["dtype"]]
     assert moe_rel(f64(out["y"]), ref["y"], f64(inp_cpu["x"]), cfg["dtype"]) < TOL_Y[cfg["dtype"]]
     return out, ref
+
+
+@pytest.mark.parametrize("T,E,k", [(256, 8, 2), (257, 8, 2), (64, 32, 8), (65, 32, 8)],
+                         ids=["one-launch-T256", "four-kernels-T257", "one-launch-TE2048",
+                              "four-kernels-TE2080"])
+def test_route_dispatch_at_the_one_launch_limits(T, E, k):
+    """Decode-sized batches route and dispatch in one launch up to T = 256,
+    T*k = 512, T*E = 2048; one token past a limit the four-kernel path takes
+    over.  Both sides of each limit match the oracle, aux loss included."""
+    cfg = workloads.config("mixtral_prefill", T=T, d=256, F=128, E=E, k=k, seed=3700 + T)
+    out, ref = _layer_vs_oracle(cfg)
+    aux = float(out["stats"][0].cpu())
+    assert abs(aux - ref["aux"]) <= TOL_AUX * abs(ref["aux"])
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])

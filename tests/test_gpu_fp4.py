@@ -20,6 +20,7 @@ CASES = {
     "gelu_capacity": dict(base="switch_skewed", T=512, d=256, F=512, E=16, k=1, seed=6003),
     "swiglu_k4": dict(base="mixtral_prefill", T=200, d=384, F=256, E=16, k=4, seed=6004),
     "one_token": dict(base="mixtral_decode", T=1, d=128, F=128, E=8, k=2, seed=6005),
+    "dense_e1": dict(base="mixtral_prefill", T=40, d=256, F=256, E=1, k=1, seed=6010),
 }
 
 

@@ -17,6 +17,7 @@ CASES = {
     "swiglu_decode": dict(base="mixtral_decode", T=5, d=256, F=384, seed=5002, weight_seed=5002),
     "gelu_capacity": dict(base="switch_skewed", T=512, d=256, F=512, E=16, k=1, seed=5003),
     "swiglu_k4": dict(base="mixtral_prefill", T=200, d=256, F=256, E=16, k=4, seed=5004),
+    "dense_e1": dict(base="mixtral_prefill", T=40, d=256, F=256, E=1, k=1, seed=5010),
 }
 
 
