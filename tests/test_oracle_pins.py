@@ -412,21 +412,58 @@ def test_aux_gradient_matches_central_differences(scoring):
             assert g[t, j] == pytest.approx(0.7 * (ap - am) / (2 * h), rel=1e-6, abs=1e-10)
 
 
-def test_aux_router_backward_products():
-    """g_Wr = g^T x and g_x = g Wr (numpy matmuls), with x, Wr in nn.Linear
-    layout; softmax rows of the logit gradient sum to zero."""
+def _dyadic(r, shape, lo, hi, bits=8):
+    """fp32 values that are multiples of 2^-bits in [lo, hi): adding or
+    subtracting 2^-20 to one of them stays exact in fp32 (|v| < 8 needs at
+    most 23 significant bits), so a finite-difference step perturbs exactly
+    the one input it names."""
+    scale = 2 ** bits
+    return (r.integers(int(lo * scale), int(hi * scale), size=shape) / scale).astype(np.float32)
+
+
+@pytest.mark.parametrize("scoring", ["softmax", "sigmoid"])
+def test_aux_router_backward_matches_central_differences(scoring):
+    """g_Wr and g_x of the oracle's router backward equal central finite
+    differences of the forward aux loss taken through the oracle's own
+    router (logits from x and Wr), scores and aux loss, with the pre-drop
+    counts f_e held fixed (they are piecewise constant).  Non-square shapes
+    (T=7, d=5, E=4), so a transposed product or a swapped operand fails; every
+    entry of Wr and of x is perturbed on its own."""
     r = _rng(32)
-    T, d, E = 9, 7, 4
-    x = r.normal(size=(T, d)).astype(np.float32)
-    Wr = r.normal(size=(E, d)).astype(np.float32)
+    T, d, E, k = 7, 5, 4, 2
+    x = _dyadic(r, (T, d), -4, 4)
+    Wr = _dyadic(r, (E, d), -0.75, 0.75)
     logits = oracle.router_logits(x, Wr)
-    idx, _, _ = oracle.topk(logits, 2)
+    idx, _, _ = oracle.topk(logits, k, scoring=scoring)
     counts = oracle.dispatch(idx, E, -1)["counts_pre"]
-    g, gW, gx = oracle.aux_router_backward(x, Wr, logits, counts)
-    np.testing.assert_allclose(g.sum(axis=1), 0.0, atol=1e-15)
-    np.testing.assert_allclose(gW, g.T @ x.astype(np.float64), rtol=1e-12, atol=1e-15)
-    np.testing.assert_allclose(gx, g @ Wr.astype(np.float64), rtol=1e-12, atol=1e-15)
+    g, gW, gx = oracle.aux_router_backward(x, Wr, logits, counts, grad_aux=0.7, scoring=scoring)
     assert gW.shape == (E, d) and gx.shape == (T, d)
+
+    def aux(xv, wv):
+        return oracle.aux_loss(counts, oracle.topk(oracle.router_logits(xv, wv), k,
+                                                   scoring=scoring)[2])
+
+    h = np.float32(2.0 ** -20)
+    fd_W = np.empty((E, d))
+    for e in range(E):
+        for i in range(d):
+            wp, wm = Wr.copy(), Wr.copy()
+            wp[e, i] += h
+            wm[e, i] -= h
+            assert wp[e, i] - Wr[e, i] == h and Wr[e, i] - wm[e, i] == h
+            fd_W[e, i] = 0.7 * (aux(x, wp) - aux(x, wm)) / (2.0 * float(h))
+    fd_x = np.empty((T, d))
+    for t in range(T):
+        for i in range(d):
+            xp, xm = x.copy(), x.copy()
+            xp[t, i] += h
+            xm[t, i] -= h
+            assert xp[t, i] - x[t, i] == h and x[t, i] - xm[t, i] == h
+            fd_x[t, i] = 0.7 * (aux(xp, Wr) - aux(xm, Wr)) / (2.0 * float(h))
+    np.testing.assert_allclose(gW, fd_W, rtol=1e-6, atol=1e-9)
+    np.testing.assert_allclose(gx, fd_x, rtol=1e-6, atol=1e-9)
+    # the differences are not vacuous: the gradients are far from zero
+    assert np.abs(fd_W).max() > 1e-3 and np.abs(fd_x).max() > 1e-3
 
 
 # ----------------------------------------------------- FP8 expert weights
