@@ -276,7 +276,13 @@ int moe_layer_forward_profiled(const moe_cfg *cfg, const void *x, const void *Wr
  *    nothing.
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture.
+ *    before any stream capture.  The address is cached per device with the
+ *    id of the context it was read in; the first call in a new context on
+ *    that device (e.g. after cudaDeviceReset) looks it up again.
+ *  - Pointer arguments are checked as moe_dispatch checks them (non-NULL
+ *    where required, int / float buffers 4-byte aligned, including stats,
+ *    prob_mean and device_status when given); a failed check returns
+ *    MOE_ERR_INVALID_ARG and launches nothing.
  *  - Every call clears the scratch's control words, then uses it; all calls
  *    in the process share the one array, so calls that overlap on the GPU
  *    (other streams, other threads) race and must be serialised by the caller.

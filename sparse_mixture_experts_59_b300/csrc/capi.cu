@@ -519,6 +519,7 @@ int run_expert_ffn(const moe_cfg& c, const DevInfo& di, const void* x, const int
 namespace moe {
 int set_last_error(int code, const char* msg) { return fail(code, "%s", msg); }
 int set_cuda_error(cudaError_t e, const char* where) { return fail_cuda(e, where); }
+int check_aligned4(const void* p, const char* name) { return check_ptr4(p, name); }
 }  // namespace moe
 
 // ====================================================================== ABI
@@ -596,6 +597,7 @@ int moe_dispatch(const moe_cfg* cfg, const int* topk_idx, const float* prob_mean
     MOE_TRY(check_ptr4(dest, "dest"));
     if (!drop_mask) return fail(MOE_ERR_INVALID_ARG, "drop_mask is NULL%s");
     if (stats) MOE_TRY(check_ptr4(stats, "stats"));
+    if (prob_mean) MOE_TRY(check_ptr4(prob_mean, "prob_mean"));
     DevInfo di;
     MOE_TRY(device_info(&di));
     return run_dispatch(*cfg, di, topk_idx, prob_mean, counts_pre, counts_kept, offsets, perm_src,

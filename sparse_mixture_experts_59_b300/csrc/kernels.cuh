@@ -19,6 +19,8 @@ inline int dispatch_blocks(int A) { return A > 0 ? (A + kDspChunk - 1) / kDspChu
 // capi.cu: record a host-side failure for moe_last_error and return `code`
 int set_last_error(int code, const char* msg);
 int set_cuda_error(cudaError_t e, const char* where);   // returns MOE_ERR_CUDA
+// MOE_OK if p is non-NULL and 4-byte aligned, else MOE_ERR_INVALID_ARG naming `name`
+int check_aligned4(const void* p, const char* name);
 
 // route.cu
 cudaError_t launch_router_logits_simt(int dtype, const void* x, const void* Wr, const float* bias,

@@ -103,3 +103,34 @@ def test_calls_check_arguments_before_launching(lib):
     nz = binding.workspace_size(z)
     assert L.moe_route(ctypes.byref(z), None, None, None, None, None, None, None, fake, nz, None) == 0
     assert L.moe_combine(ctypes.byref(z), None, None, None, None, None, None) == 0
+
+
+def test_noalloc_dispatch_rejects_misaligned_pointers_before_launching(lib):
+    """moe_dispatch_noalloc checks its pointers as moe_dispatch does: a NULL or
+    misaligned int / float buffer returns MOE_ERR_INVALID_ARG naming it, before
+    any CUDA call (the addresses below are never dereferenced)."""
+    c = binding.make_config(workloads.config("mixtral_prefill", T=64, d=64, F=64, E=8, k=2))
+    good = [0x100000 + 0x1000 * i for i in range(11)]
+    names = ("topk_idx", "prob_mean", "counts_pre", "counts_kept", "offsets", "perm_src", "dest",
+             "drop_mask", "stats", "device_status")
+    for j, name in enumerate(names):
+        if name == "drop_mask":
+            continue                       # bytes: any address is aligned
+        args = list(good[:10])
+        args[j] = good[j] + 2
+        rc = lib.moe_dispatch_noalloc(ctypes.byref(c), *[ctypes.c_void_p(a) for a in args], None)
+        assert rc == 1, name
+        assert name in lib.moe_last_error().decode(), name
+    args = list(good[:10])
+    args[names.index("dest")] = 0
+    rc = lib.moe_dispatch_noalloc(ctypes.byref(c), *[ctypes.c_void_p(a) for a in args], None)
+    assert rc == 1 and "dest" in lib.moe_last_error().decode()
+
+
+def test_dispatch_rejects_misaligned_prob_mean(lib):
+    c = binding.make_config(workloads.config("mixtral_prefill", T=64, d=64, F=64, E=8, k=2))
+    ws_bytes = binding.workspace_size(c)
+    p = [ctypes.c_void_p(0x100000 + 0x1000 * i) for i in range(10)]
+    p[1] = ctypes.c_void_p(0x100000 + 0x1000 + 1)          # prob_mean
+    rc = lib.moe_dispatch(ctypes.byref(c), *p[:9], ctypes.c_void_p(0x200000), ws_bytes, None)
+    assert rc == 1 and "prob_mean" in lib.moe_last_error().decode()

@@ -54,3 +54,32 @@ def test_noalloc_dispatch_refuses_sizes_beyond_its_scratch():
     with pytest.raises(binding.MoeError) as ei:
         binding.dispatch_noalloc(cfg, idx)
     assert ei.value.code == 1 and "65536" in str(ei.value)
+
+
+def test_noalloc_dispatch_reports_a_device_error_then_recovers():
+    """A call given an expert index outside [0, E) reports MOE_ERR_DEVICE_BOUNDS
+    in its device_status output (the kernel leaves that assignment out of every
+    count); the next call clears the shared scratch itself, returns status 0
+    and matches moe_dispatch bit for bit."""
+    T, E, k = 300, 8, 2
+    cfg = binding.make_config(workloads.config("mixtral_prefill", T=T, d=64, F=64, E=E, k=k))
+    idx = torch.randint(0, E, (T, k), dtype=torch.int32)
+    idx[:, 1] = (idx[:, 0] + 1) % E
+    bad = idx.clone()
+    bad[17, 0] = E
+    got = binding.dispatch_noalloc(cfg, bad.cuda())
+    torch.cuda.synchronize()
+    assert int(got["device_status"].item()) == 6          # MOE_ERR_DEVICE_BOUNDS
+    assert int(got["counts_pre"].sum().item()) == T * k - 1
+    ws = binding.new_workspace(cfg)
+    ref = binding.dispatch(cfg, idx.cuda(), ws=ws)
+    got = binding.dispatch_noalloc(cfg, idx.cuda())
+    torch.cuda.synchronize()
+    assert int(got["device_status"].item()) == 0
+    assert binding.device_status(ws) == 0
+    R = int(ref["offsets"][-1].item())
+    for key in KEYS:
+        a, b = got[key].cpu(), ref[key].cpu()
+        if key == "perm_src":
+            a, b = a[:R], b[:R]
+        assert torch.equal(a, b), key
