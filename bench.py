@@ -18,9 +18,7 @@ oracle/) on a bounded sample of the same workload, as the baseline arm.
 import argparse
 import json
 import os
-import subprocess
 import sys
-import tempfile
 import time
 
 import numpy as np
@@ -66,6 +64,11 @@ def parse_args():
                      help="the main workload with FP8 E4M3 expert weights (profiling cases)")
     low.add_argument("--fp4", action="store_true",
                      help="the main workload with packed 4-bit (E2M1) expert weights")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the fine-grained, Switch-skewed and tiny fp32 workloads")
+    ap.add_argument("--sustained-seconds", type=float, default=2.5,
+                    help="length of the back-to-back loop timed against the sustained peak "
+                         "(0 = skip)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--sweep", default=None,
                     help="comma-separated token counts: time the layer at each T on the "
@@ -147,68 +150,89 @@ def measured_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-class ClockSampler:
-    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+_REASON_BITS = (("gpu_idle", 0x1), ("sw_power_cap", 0x4), ("hw_slowdown", 0x8),
+                ("sw_thermal_slowdown", 0x20), ("hw_thermal_slowdown", 0x40),
+                ("hw_power_brake_slowdown", 0x80))
 
-    def __init__(self, gpu_index):
-        self.idx = gpu_index
-        self.proc = None
-        self.path = None
+
+class ClockSampler:
+    """SM clock, power and clock-event reasons of one GPU, sampled about every
+    2 ms by NVML in a background thread while a timed region runs (a timed
+    region of 20 layer calls lasts ~40 ms, so a 100 ms nvidia-smi poll would
+    mostly see the idle GPU around it).  Without NVML the summary is None.
+    The summary's sm_mhz is the median over samples taken while the GPU was
+    busy (NVML's gpu_idle reason clear)."""
+
+    def __init__(self, device_index, period_s=0.002):
+        self.idx = device_index
+        self.period = period_s
+        self.rows = []
+        self.thread = None
+        self.handle = None
+        self.nvml = None
+
+    def _handle(self):
+        import pynvml
+        pynvml.nvmlInit()
+        self.nvml = pynvml
+        try:
+            uuid = str(torch.cuda.get_device_properties(self.idx).uuid)
+            return pynvml.nvmlDeviceGetHandleByUUID(("GPU-" + uuid) if not uuid.startswith("GPU-") else uuid)
+        except Exception:
+            return pynvml.nvmlDeviceGetHandleByIndex(self.idx)
 
     def start(self):
+        import threading
+        self.rows = []
         try:
-            fd, self.path = tempfile.mkstemp(suffix=".csv")
-            os.close(fd)
-            self.fh = open(self.path, "w")
-            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.FIELDS,
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
-                                         stdout=self.fh, stderr=subprocess.DEVNULL)
-            time.sleep(0.3)
+            self.handle = self._handle()
         except Exception:
-            self.proc = None
+            self.handle = None
+            return
+        nv = self.nvml
+        get_reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.max_mhz = float(nv.nvmlDeviceGetMaxClockInfo(self.handle, nv.NVML_CLOCK_SM))
+        self.stop_flag = threading.Event()
+
+        def loop():
+            n = 0
+            while not self.stop_flag.is_set():
+                try:
+                    sm = nv.nvmlDeviceGetClockInfo(self.handle, nv.NVML_CLOCK_SM)
+                    rs = get_reasons(self.handle)
+                    pw = nv.nvmlDeviceGetPowerUsage(self.handle) / 1000.0 if n % 4 == 0 else None
+                    self.rows.append((time.perf_counter(), float(sm), int(rs), pw))
+                except Exception:
+                    pass
+                n += 1
+                time.sleep(self.period)
+
+        self.thread = threading.Thread(target=loop, daemon=True)
+        self.thread.start()
 
     def stop(self):
-        if self.proc is None:
+        if self.thread is None:
             return None
-        time.sleep(0.15)
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except Exception:
-            self.proc.kill()
-        self.fh.close()
-        rows = []
-        with open(self.path) as fh:
-            for line in fh:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9 or parts[0] != str(self.idx):
-                    continue
-                rows.append(parts)
-        os.remove(self.path)
+        self.stop_flag.set()
+        self.thread.join(timeout=5)
+        self.thread = None
+        rows = self.rows
         if not rows:
             return None
-
-        def num(s):
-            try:
-                return float(s)
-            except ValueError:
-                return float("nan")
-        sm = np.array([num(r[1]) for r in rows])
-        mx = np.array([num(r[2]) for r in rows])
+        busy = [r for r in rows if not (r[2] & 0x1)]
+        use = busy if busy else rows
+        sm = np.array([r[1] for r in use])
         reasons = set()
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for r in rows:
-            for name, val in zip(names, r[5:9]):
-                if val.strip().lower() in ("active", "1"):
+        for r in use:
+            for name, bit in _REASON_BITS:
+                if name != "gpu_idle" and (r[2] & bit):
                     reasons.add(name)
-        busy = sm[sm >= np.nanmedian(sm) * 0.5] if len(sm) else sm
-        return {"sm_mhz": float(np.nanmedian(busy)) if len(busy) else None,
-                "sm_max_mhz": float(np.nanmax(mx)) if len(mx) else None,
-                "reasons": sorted(reasons), "samples": len(rows),
-                "power_w_max": float(np.nanmax([num(r[3]) for r in rows]))}
+        power = [r[3] for r in rows if r[3] is not None]
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": self.max_mhz,
+                "sm_mhz_p10": float(np.percentile(sm, 10)), "sm_mhz_p90": float(np.percentile(sm, 90)),
+                "reasons": sorted(reasons), "samples": len(rows), "samples_busy": len(busy),
+                "power_w_max": float(max(power)) if power else None, "source": "nvml, ~2 ms period"}
 
 
 # ------------------------------------------------------------ our path
@@ -278,7 +302,41 @@ def workload_config(args):
         over["T"] = args.tokens
     if args.experts is not None:
         over["E"] = args.experts
+    if args.gemm:
+        over["gemm_kernel"] = args.gemm
     return workloads.config(args.workload, **over)
+
+
+def weight_bytes(cfg, counts_kept):
+    """Bytes of expert weights a layer call must stream: every routed expert
+    that kept at least one assignment (its W1, W3, W2 and biases; codes,
+    block and row scales for low-bit weights) plus the shared expert."""
+    d, F = cfg["d"], cfg["F"]
+    mats = 3 if cfg["act"] == "swiglu" else 2
+    if cfg.get("weight_fp4"):
+        per = int(mats * d * F * 80 / 128) + (2 * F + d) * 4
+    elif cfg.get("weight_fp8"):
+        per = mats * d * F + (2 * F + d) * 4
+    else:
+        es = 4 if cfg["dtype"] == "f32" else 2
+        per = (mats * d * F + ((F + d) if cfg["has_bias"] else 0)) * es
+    hit = int((np.asarray(counts_kept) > 0).sum())
+    Fs = cfg.get("F_shared", 0) or 0
+    return hit * per + 3 * d * Fs * (4 if cfg["dtype"] == "f32" else 2), hit
+
+
+def gemm_roofline(alg, wbytes, gemm_s, peaks):
+    """The grouped GEMMs' roofline time max(flop / tensor peak, weight bytes /
+    HBM peak) at the burst tensor peak (the GEMMs are timed over tens of
+    milliseconds), and the fraction of it the measured time reaches."""
+    tf = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    bw = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    t_c = (alg["up"] + alg["down"]) / (tf * 1e12)
+    t_m = wbytes / (bw * 1e9)
+    t_r = max(t_c, t_m)
+    return {"bound": "tensor" if t_c >= t_m else "hbm", "roofline_ms": round(t_r * 1e3, 4),
+            "compute_ms": round(t_c * 1e3, 4), "bytes_ms": round(t_m * 1e3, 4),
+            "frac": round(t_r / gemm_s, 4), "tensor_peak_tflops": tf, "hbm_peak_gbs": bw}
 
 
 def run_ours(args, world, rank, local):
@@ -305,21 +363,26 @@ def run_ours(args, world, rank, local):
 
     up_s = stages["up_gemm"] / 1e3
     dn_s = stages["down_gemm"] / 1e3
-    peak_tf = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    # the timed region lasts tens of milliseconds: the burst peak applies
+    burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
     up_tf = alg["up"] / up_s / 1e12
     kname = "up_gemm/%s" % (args.gemm or "auto")
     traffic, digest = recorded_traffic(args.workload, kname) if args.tokens is None and \
         args.experts is None else (None, None)
+    mhz = clk["sm_mhz"] if clk else None
     roof = {"kernel": "up-projection grouped GEMM (SwiGLU epilogue)", "bound": "tensor",
-            "achieved": round(up_tf, 1), "peak": peak_tf, "unit": "TFLOP/s",
-            "frac": round(up_tf / peak_tf, 4), "traffic": traffic,
+            "achieved": round(up_tf, 1), "peak": burst, "unit": "TFLOP/s",
+            "frac": round(up_tf / burst, 4), "traffic": traffic,
             "traffic_note": "ncu dram__bytes_read.sum + dram__bytes_write.sum per launch, "
                             "profiles/traffic_%s.txt; null if the kernel sources changed "
                             "since (sources digest %s)" % (args.workload, digest),
-            "peak_source": "%s bf16_tflops_sustained" % peak_src,
+            "peak_source": "%s bf16_tflops (burst: the timed region is %d layer calls, "
+                           "%.0f ms)" % (peak_src, args.steps, ms * args.steps),
             "algorithmic_flop_per_launch": alg["up"], "launch_ms": round(stages["up_gemm"], 4),
-            "frac_of_burst_peak": round(up_tf / peaks.get("bf16_tflops", 1816.0), 4)}
+            "launch_mcycles_at_median_sm_clock": round(stages["up_gemm"] * mhz / 1e3, 4)
+            if mhz else None}
     gg_tf = (alg["up"] + alg["down"]) / (up_s + dn_s) / 1e12
+    wbytes, hit = weight_bytes(cfg, outputs["counts_kept"].cpu().numpy())
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
@@ -336,9 +399,11 @@ def run_ours(args, world, rank, local):
                    "parallelism": "replicas" if world > 1 else "single",
                    "gemm_kernel": args.gemm or "auto"},
         "roofline": roof,
-        "grouped_gemm": {"tflops": round(gg_tf, 1), "frac_of_peak": round(gg_tf / peak_tf, 4),
-                         "peak": peak_tf, "up_ms": round(stages["up_gemm"], 4),
-                         "down_ms": round(stages["down_gemm"], 4)},
+        "grouped_gemm": {"tflops": round(gg_tf, 1), "frac_of_peak": round(gg_tf / burst, 4),
+                         "peak": burst, "up_ms": round(stages["up_gemm"], 4),
+                         "down_ms": round(stages["down_gemm"], 4),
+                         "down_tflops": round(alg["down"] / dn_s / 1e12, 1),
+                         "roofline": gemm_roofline(alg, wbytes, up_s + dn_s, peaks)},
         "stage_ms": {k: round(v, 4) for k, v in stages.items()},
         "timing": "value from %d plain layer calls; stage_ms and the roofline's launch_ms from "
                   "%d more calls with CUDA events at the stage boundaries" % (args.steps, args.steps),
@@ -347,17 +412,129 @@ def run_ours(args, world, rank, local):
         "pdl": os.environ.get("MOE_PDL", "1") != "0",
         "clocks": clk,
     }
-
+    if args.sustained_seconds > 0:
+        result["sustained"] = run_sustained(layer, x, outputs, cfg, alg, args, world, peaks,
+                                            peak_src, local)
     if not args.no_e2e:
         result["e2e"] = run_e2e(layer, cfg, x, args, world, dev)
+    del layer
     if not args.no_decode:
         result["decode"] = run_decode(args, bf16_inp, world, dev, peaks, peak_src)
         result["decode_fp8"] = run_decode(args, bf16_inp, world, dev, peaks, peak_src, low="fp8")
         result["decode_fp4"] = run_decode(args, bf16_inp, world, dev, peaks, peak_src, low="fp4")
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(inp, cfg, args.cpu_seconds)
-    del layer
+    del inp, bf16_inp
+    torch.cuda.empty_cache()
+    if not args.no_configs:
+        for name in ("fine_grained", "switch_skewed", "tiny_fp32"):
+            result[name] = run_workload(name, args, world, dev, peaks, local)
+            torch.cuda.empty_cache()
     return result
+
+
+def run_sustained(layer, x, outputs, cfg, alg, args, world, peaks, peak_src, local):
+    """Back-to-back layer calls for about args.sustained_seconds, each with
+    stage events, with their own clock record: the up-projection against the
+    sustained bf16 peak (a seconds-long loop under the power cap), and its
+    time in SM cycles at the median clock so the clock dependence shows."""
+    probe = time.perf_counter()
+    layer.forward(x, outputs=outputs)
+    torch.cuda.synchronize()
+    one = max(time.perf_counter() - probe, 1e-4)
+    n = int(min(5000, max(50, args.sustained_seconds / one)))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(n)]
+    clocks = ClockSampler(local)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks.start()
+    start.record()
+    for i in range(n):
+        layer.forward(x, outputs=outputs, events=evs[i])
+    end.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if binding.device_status(layer.ws) != 0:
+        raise RuntimeError("device status after the sustained loop")
+    total_ms = start.elapsed_time(end)
+    up = np.array([r[3].elapsed_time(r[4]) for r in evs])
+    dn = np.array([r[4].elapsed_time(r[5]) for r in evs])
+    peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    up_tf = alg["up"] / (up.mean() / 1e3) / 1e12
+    mhz = clk["sm_mhz"] if clk else None
+    return {"seconds": round(total_ms / 1e3, 3), "steps": n, "ms_per_step": round(total_ms / n, 4),
+            "tokens_per_s": round(cfg["T"] * n / (total_ms / 1e3), 1),
+            "up_gemm_ms": round(float(up.mean()), 4), "down_gemm_ms": round(float(dn.mean()), 4),
+            "up_tflops": round(up_tf, 1), "peak": peak, "frac": round(up_tf / peak, 4),
+            "peak_source": "%s bf16_tflops_sustained" % peak_src,
+            "up_gemm_mcycles_at_median_sm_clock": round(float(up.mean()) * mhz / 1e3, 4) if mhz else None,
+            "timing": "every call records events at its stage boundaries", "clocks": clk}
+
+
+def time_layer_flushed(layer, x, steps, warmup, outputs, flush):
+    """Mean layer time over `steps` calls with an L2 flush (a write of
+    `flush`, larger than L2) before each; only the call is inside its events."""
+    for _ in range(warmup):
+        layer.forward(x, outputs=outputs)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    torch.cuda.synchronize()
+    for a, b in evs:
+        flush.fill_(1)
+        a.record()
+        layer.forward(x, outputs=outputs)
+        b.record()
+    torch.cuda.synchronize()
+    return float(np.mean([a.elapsed_time(b) for a, b in evs]))
+
+
+def run_workload(name, args, world, dev, peaks, local):
+    """Another of the five workloads at its full size: layer time, tokens/s,
+    the grouped GEMMs against their roofline (flop at the burst tensor peak,
+    weight bytes of the experts hit at the HBM peak), drops and aux loss."""
+    cfg = workloads.config(name)
+    inp = workloads.make_inputs(cfg, device=dev)
+    layer = binding.MoeLayer(cfg, inp, device=dev)
+    x = inp["x"]
+    outputs = {"y": torch.empty_like(x),
+               "counts_kept": torch.empty(cfg["E"], dtype=torch.int32, device=dev),
+               "stats": torch.empty(2, dtype=torch.float32, device=dev)}
+    steps = max(10, min(args.steps, 20))
+    clocks = ClockSampler(local)
+    ms, stages, clk = time_layer(layer, x, steps, args.warmup, world, outputs, clocks)
+    out = {"workload": name, "T": cfg["T"], "d_model": cfg["d"], "d_ff": cfg["F"],
+           "experts": cfg["E"], "top_k": cfg["k"], "act": cfg["act"],
+           "F_shared": cfg.get("F_shared", 0), "dtype": cfg["dtype"],
+           "capacity": "dropless" if not cfg["capacity_factor"] else cfg["capacity_factor"]}
+    wbytes, hit = weight_bytes(cfg, outputs["counts_kept"].cpu().numpy())
+    if wbytes < 2 * 126e6:
+        # inputs smaller than L2: time again with an L2 flush before each call
+        flush = torch.empty(256 * 2 ** 20 // 4, dtype=torch.float32, device=dev)
+        ms_flushed = time_layer_flushed(layer, x, steps, args.warmup, outputs, flush)
+        out["ms_per_step_l2_flushed"] = round(ms_flushed, 4)
+        out["us_per_layer_l2_flushed"] = round(ms_flushed * 1e3, 2)
+        del flush
+    R = int(outputs["counts_kept"].sum().item())
+    stats = outputs["stats"].cpu().numpy()
+    alg = algorithmic(cfg, R)
+    gemm_s = (stages["up_gemm"] + stages["down_gemm"]) / 1e3
+    out.update({
+        "ms_per_step": round(ms, 4), "tokens_per_s": round(cfg["T"] * world / (ms / 1e3), 1),
+        "steps": steps, "kept_rows": R, "experts_hit": hit, "weight_bytes": wbytes,
+        "drop_fraction": round(float(stats[1]), 6), "aux_loss": round(float(stats[0]), 6),
+        "gemm_ms": round(gemm_s * 1e3, 4),
+        "gemm_tflops": round((alg["up"] + alg["down"]) / gemm_s / 1e12, 1),
+        "up_tflops": round(alg["up"] / (stages["up_gemm"] / 1e3) / 1e12, 1),
+        "down_tflops": round(alg["down"] / (stages["down_gemm"] / 1e3) / 1e12, 1),
+        "weight_gbs": round(wbytes / gemm_s / 1e9, 1),
+        "layer_tflops": round(alg["total"] / (ms / 1e3) / 1e12, 2),
+        "stage_ms": {k: round(v, 4) for k, v in stages.items()},
+        "clocks": clk})
+    if cfg["dtype"] == "bf16":
+        out["gemm_roofline"] = gemm_roofline(alg, wbytes, gemm_s, peaks)
+    del layer, inp, outputs
+    return out
 
 
 def run_e2e(layer, cfg, x, args, world, dev):
@@ -438,13 +615,7 @@ def run_decode(args, prefill_inp, world, dev, peaks, peak_src, low=None):
     steps = max(20, args.steps)
     ms, stages, _ = time_layer(layer, inp["x"], steps, args.warmup, world, outputs)
     ms = max_over_ranks(ms, world)
-    counts = outputs["counts_kept"].cpu().numpy()
-    hit = int((counts > 0).sum())
-    # weight bytes per routed expert: codes (+ block scales) + fp32 row scales
-    code_bytes = {None: 2.0, "fp8": 1.0, "fp4": 80.0 / 128.0}[low]
-    per_expert = int(3 * cfg["d"] * cfg["F"] * code_bytes) + \
-        (2 * cfg["F"] + cfg["d"]) * 4 * (low is not None)
-    wbytes = hit * per_expert
+    wbytes, hit = weight_bytes(cfg, outputs["counts_kept"].cpu().numpy())
     gemm_s = (stages["up_gemm"] + stages["down_gemm"]) / 1e3
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     gbs = wbytes / gemm_s / 1e9
@@ -554,10 +725,7 @@ def run_sweep(args, world, local):
         inp["cfg"] = cfg
         entry = {"T": T}
         for g in ("auto", "tc1", "swap", "pair"):
-            if g == "auto":
-                os.environ.pop("MOE_GEMM_KERNEL", None)
-            else:
-                os.environ["MOE_GEMM_KERNEL"] = g
+            cfg = dict(base, T=T, gemm_kernel=g)
             layer = binding.MoeLayer(cfg, inp, device=dev)
             outputs = {"y": torch.empty_like(inp["x"]),
                        "counts_kept": torch.empty(cfg["E"], dtype=torch.int32, device=dev)}
@@ -572,7 +740,6 @@ def run_sweep(args, world, local):
                         "gemm_tflops": round((alg["up"] + alg["down"]) / (gemm_ms / 1e3) / 1e12, 1),
                         "weight_gbs": round(hit * per_expert / (gemm_ms / 1e3) / 1e9, 1)}
             del layer
-        os.environ.pop("MOE_GEMM_KERNEL", None)
         rows.append(entry)
     return {"sweep": args.workload, "d_model": base["d"], "d_ff": base["F"], "experts": base["E"],
             "top_k": base["k"], "hbm_peak_gbs": peaks.get("hbm_gbs"),
@@ -587,8 +754,6 @@ def main():
         if rank == 0:
             print(json.dumps(res), flush=True)
         return
-    if args.gemm:
-        os.environ["MOE_GEMM_KERNEL"] = args.gemm
     if args.no_pdl:
         os.environ["MOE_PDL"] = "0"
     world, rank, local = dist_init()

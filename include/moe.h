@@ -71,6 +71,8 @@ enum moe_status {
 enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 };
 enum moe_act { MOE_GELU_ERF = 0, MOE_SWIGLU = 1 };
 enum moe_scoring { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 };
+enum moe_gemm_kernel { MOE_GEMM_AUTO = 0, MOE_GEMM_TC1 = 1, MOE_GEMM_PAIR = 2, MOE_GEMM_SWAP = 3 };
+enum moe_route_path { MOE_ROUTE_AUTO = 0, MOE_ROUTE_SEPARATE = 1 };
 
 /* Layer shape and options.
  *  T        tokens (>= 0; T = 0 is a no-op)
@@ -106,7 +108,21 @@ enum moe_scoring { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 };
  *           values 16b .. 16b+15), 8 zero bytes -- with the fp32 row scales
  *           s1, s3, s2 on top: w = code * block scale * row scale.  bf16
  *           layers without a shared expert; d and F multiples of 128.
- * A zero-filled moe_cfg with the sizes set gives the pages' default router. */
+ *  gemm_kernel  bf16 expert GEMM kernel: MOE_GEMM_AUTO (default) picks one from
+ *           the shape; MOE_GEMM_TC1 (tokens on the MMA's M, 128-row tiles, one
+ *           SM per tile), MOE_GEMM_PAIR (tokens on M, 256-row tiles on SM
+ *           pairs) or MOE_GEMM_SWAP (weights on M, tokens on N, SM pairs) forces
+ *           one.  All give results within the bf16 tolerance of each other;
+ *           ignored by fp32 and low-bit layers.
+ *  route_path MOE_ROUTE_AUTO (default): decode-sized batches (T <= 256,
+ *           T*k <= 512, T*E <= 2048) route and dispatch in one launch;
+ *           MOE_ROUTE_SEPARATE: always the separate router and dispatch kernels.
+ * A zero-filled moe_cfg with the sizes set gives the pages' default router and
+ * the automatic kernel choices.
+ *
+ * Environment: MOE_PDL=0, read once per process, launches every kernel
+ * without programmatic dependent launch (each kernel then starts only after
+ * its predecessor has finished); results are the same either way. */
 typedef struct moe_cfg {
     int T, d, F, E, k;
     int F_shared;
@@ -118,6 +134,8 @@ typedef struct moe_cfg {
     int no_renorm;
     int weight_fp8;
     int weight_fp4;
+    int gemm_kernel;
+    int route_path;
 } moe_cfg;
 
 /* Expert weights (device pointers, dtype of the layer).  W3 only for SwiGLU;
@@ -184,7 +202,7 @@ int moe_workspace_init(const moe_cfg *cfg, void *ws, size_t ws_bytes, void *stre
  * T <= 256 with T*k <= 512 and T*E <= 2048, take K-sliced sums on CUDA cores;
  * larger bf16 batches tensor-core tiles, larger fp32 ones a tiled CUDA-core
  * GEMM), and moe_layer_forward uses the same order as this call, so both give
- * the same bits.  MOE_SMALL_FRONT=0 in the environment takes the large-batch
+ * the same bits.  cfg->route_path = MOE_ROUTE_SEPARATE takes the large-batch
  * path at every size. */
 int moe_route(const moe_cfg *cfg, const void *x, const void *Wr, const float *logit_bias,
               float *logits, int *topk_idx, float *topk_w, float *prob_mean,
@@ -306,6 +324,19 @@ int moe_get_device_status(void *ws, size_t ws_bytes, void *stream, int *status);
  * device status; their outputs are then not meaningful.  The hook clears
  * itself; re-initialise the workspace before further use. */
 int moe_test_hold_lookback_block(void *ws, size_t ws_bytes, int block, void *stream);
+
+/* Test hook for the failure path of the expert GEMMs' bounded waits (no
+ * counterpart on the pages).  From the next layer call on this workspace, the
+ * up-projection GEMM's weight producer in every CTA that reaches shared-memory
+ * ring iteration `iteration` (0-based, counted over the CTA's tiles and K
+ * blocks) stops there without loading it and without reporting anything, as
+ * if the copy had been lost.  The MMA issuer's (or, for FP8 / 4-bit weights,
+ * the converters') wait for that stage runs out after about a second; the
+ * kernel records MOE_ERR_DEVICE_TIMEOUT, waits for its own copies and MMAs in
+ * flight, frees its tensor memory and returns, and the layer's outputs are not
+ * meaningful.  The hook stays set until moe_workspace_init, which is needed
+ * before further use anyway. */
+int moe_test_hold_gemm_stage(void *ws, size_t ws_bytes, int iteration, void *stream);
 
 #ifdef __cplusplus
 }

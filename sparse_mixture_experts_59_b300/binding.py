@@ -22,7 +22,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 EXPORTS = ("moe_status_string", "moe_last_error", "moe_capacity", "moe_workspace_size",
            "moe_workspace_init", "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine",
            "moe_layer_forward", "moe_layer_forward_profiled", "moe_get_device_status",
-           "moe_dispatch_noalloc", "moe_test_hold_lookback_block", "moe_aux_loss_backward")
+           "moe_dispatch_noalloc", "moe_test_hold_lookback_block", "moe_test_hold_gemm_stage",
+           "moe_aux_loss_backward")
 
 
 class MoeError(RuntimeError):
@@ -38,7 +39,12 @@ class MoeConfig(ctypes.Structure):
                 ("dtype", ctypes.c_int), ("act", ctypes.c_int), ("has_bias", ctypes.c_int),
                 ("capacity_factor", ctypes.c_float), ("scoring", ctypes.c_int),
                 ("no_renorm", ctypes.c_int), ("weight_fp8", ctypes.c_int),
-                ("weight_fp4", ctypes.c_int)]
+                ("weight_fp4", ctypes.c_int), ("gemm_kernel", ctypes.c_int),
+                ("route_path", ctypes.c_int)]
+
+
+GEMM_KERNELS = {"auto": 0, "tc1": 1, "pair": 2, "swap": 3}
+ROUTE_PATHS = {"auto": 0, "separate": 1}
 
 
 WEIGHT_KEYS = ("W1", "W3", "W2", "b1", "b2", "S1", "S3", "S2", "s1", "s3", "s2")
@@ -82,6 +88,7 @@ def lib():
         L.moe_get_device_status.argtypes = [P, S, P, ctypes.POINTER(I)]
         L.moe_dispatch_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P]
         L.moe_test_hold_lookback_block.argtypes = [P, S, I, P]
+        L.moe_test_hold_gemm_stage.argtypes = [P, S, I, P]
         L.moe_aux_loss_backward.argtypes = [P, P, P, P, P, ctypes.c_float, P, P, P, P]
         for name in EXPORTS:
             getattr(L, name).restype = getattr(L, name).restype or I
@@ -95,7 +102,9 @@ def _check(rc):
 
 
 def make_config(cfg: dict) -> MoeConfig:
-    """C config from a workload dict (keys T, d, F, E, k, act, dtype, ...)."""
+    """C config from a workload dict (keys T, d, F, E, k, act, dtype, ...;
+    optional gemm_kernel "auto" | "tc1" | "pair" | "swap" and route_path
+    "auto" | "separate")."""
     return MoeConfig(
         T=int(cfg["T"]), d=int(cfg["d"]), F=int(cfg["F"]), E=int(cfg["E"]), k=int(cfg["k"]),
         F_shared=int(cfg.get("F_shared", 0) or 0),
@@ -106,7 +115,9 @@ def make_config(cfg: dict) -> MoeConfig:
         scoring=MOE_SCORE_SIGMOID if cfg.get("scoring", "softmax") == "sigmoid" else MOE_SCORE_SOFTMAX,
         no_renorm=0 if cfg.get("renorm", True) else 1,
         weight_fp8=int(bool(cfg.get("weight_fp8", False))),
-        weight_fp4=int(bool(cfg.get("weight_fp4", False))))
+        weight_fp4=int(bool(cfg.get("weight_fp4", False))),
+        gemm_kernel=GEMM_KERNELS[cfg.get("gemm_kernel", "auto") or "auto"],
+        route_path=ROUTE_PATHS[cfg.get("route_path", "auto") or "auto"])
 
 
 def _p(t):
@@ -286,6 +297,14 @@ def test_hold_lookback_block(ws, block, stream=None):
     """Test hook: the next dispatch on `ws` runs with look-back block `block`
     never publishing, so later blocks time out (MOE_ERR_DEVICE_TIMEOUT)."""
     _check(lib().moe_test_hold_lookback_block(_p(ws), ws.numel(), int(block), _stream(stream)))
+
+
+def test_hold_gemm_stage(ws, iteration, stream=None):
+    """Test hook: from the next layer call on `ws`, the up-projection GEMM's
+    weight producer stops before ring iteration `iteration`, so the kernel's
+    bounded waits run out (MOE_ERR_DEVICE_TIMEOUT) until the workspace is
+    re-initialised."""
+    _check(lib().moe_test_hold_gemm_stage(_p(ws), ws.numel(), int(iteration), _stream(stream)))
 
 
 def device_status(ws, stream=None) -> int:

@@ -118,6 +118,10 @@ int check_cfg(const moe_cfg* c) {
         return fail(MOE_ERR_INVALID_ARG, "4-bit expert weights need d and F multiples of 128 (80-byte chunks)%s");
     if (c->weight_fp8 && (c->d % 16 || c->F % 16))
         return fail(MOE_ERR_INVALID_ARG, "FP8 expert weights need d and F multiples of 16 (16-byte rows)%s");
+    if (c->gemm_kernel < MOE_GEMM_AUTO || c->gemm_kernel > MOE_GEMM_SWAP)
+        return fail(MOE_ERR_INVALID_ARG, "unknown gemm_kernel%s");
+    if (c->route_path != MOE_ROUTE_AUTO && c->route_path != MOE_ROUTE_SEPARATE)
+        return fail(MOE_ERR_INVALID_ARG, "unknown route_path%s");
     return MOE_OK;
 }
 
@@ -239,12 +243,9 @@ int encode_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, 
     return MOE_OK;
 }
 
-// Decode-sized batches route and dispatch in one launch (front_small.cu);
-// MOE_SMALL_FRONT=0 keeps the separate router and dispatch kernels.
-bool small_front_enabled() {
-    const char* env = getenv("MOE_SMALL_FRONT");
-    return !(env && env[0] == '0');
-}
+// Decode-sized batches route and dispatch in one launch (front_small.cu)
+// unless the config asks for the separate router and dispatch kernels.
+bool small_front_enabled(const moe_cfg& c) { return c.route_path == MOE_ROUTE_AUTO; }
 
 // Kernel for the bf16 expert GEMMs:
 //   kGemmTc1   1-SM kernel, tokens on M in 128-row tiles (ffn_tc.cu)
@@ -255,17 +256,13 @@ bool small_front_enabled() {
 // of at most 256 rows on average that fit one token tile (capacity-limited
 // layers) -> swap; long segments (>= 512 rows) -> swap; segments a little
 // over one 256-token tile, which swap would cover with a second tile that
-// re-streams the weights, and decode-sized segments -> tc1.  The environment
-// variable MOE_GEMM_KERNEL=tc1|pair|swap forces one (MOE_GEMM_PAIR=1: pair).
+// re-streams the weights, and decode-sized segments -> tc1.  cfg.gemm_kernel
+// forces one.
 enum GemmKernel { kGemmTc1, kGemmPair, kGemmSwap };
 GemmKernel choose_gemm(const moe_cfg& c) {
-    const char* env = getenv("MOE_GEMM_KERNEL");
-    if (env && !strcmp(env, "tc1")) return kGemmTc1;
-    if (env && !strcmp(env, "pair")) return kGemmPair;
-    if (env && !strcmp(env, "swap")) return kGemmSwap;
-    const char* pair = getenv("MOE_GEMM_PAIR");
-    if (pair && pair[0] == '1') return kGemmPair;
-    if (pair && pair[0] == '0') return kGemmTc1;
+    if (c.gemm_kernel == MOE_GEMM_TC1) return kGemmTc1;
+    if (c.gemm_kernel == MOE_GEMM_PAIR) return kGemmPair;
+    if (c.gemm_kernel == MOE_GEMM_SWAP) return kGemmSwap;
     const long long rows = (long long)c.T * c.k;
     const long long cap = moe_capacity(&c);
     if (cap >= 0 && cap <= 256 && rows >= 32LL * c.E) return kGemmSwap;   // one tile each
@@ -282,7 +279,7 @@ int run_route(const moe_cfg& c, const DevInfo& di, const void* x, const void* Wr
               void* ws, cudaStream_t st) {
     const Layout L = layout_of(c);
     const FrontSmallPlan fp = front_small_plan(c.T, c.d, c.E, c.k);
-    if (fp.ok && small_front_enabled()) {
+    if (fp.ok && small_front_enabled(c)) {
         // decode-sized batch: the route part of the one-launch front, so that
         // this call and the layer call give the same logits
         FrontSmallArgs a{};
@@ -384,6 +381,7 @@ int run_expert_ffn(const moe_cfg& c, const DevInfo& di, const void* x, const int
         up.status = status;
         up.wscale = w.s1;
         up.wscale2 = c.act == MOE_SWIGLU ? w.s3 : nullptr;
+        up.hold = at<int>(ws, L.ctrl) + kCtrlHoldGemm;
         MOE_CUDA(launch_ffn_fp8(up_mode, maps, up, di.num_sms, st, fp4), "up-projection launch");
         if (ev) MOE_CUDA(cudaEventRecord(ev[1], st), "event record");
         MOE_TRY(encode_rows(&maps[0], H, (uint64_t)A, c.F, "hidden rows", 16,
@@ -441,6 +439,7 @@ int run_expert_ffn(const moe_cfg& c, const DevInfo& di, const void* x, const int
     up.out = H; up.out_sh = Hsh;
     up.bias = c.has_bias ? (const __nv_bfloat16*)w.b1 : nullptr;
     up.status = status;
+    up.hold = at<int>(ws, L.ctrl) + kCtrlHoldGemm;
     TcFfnArgs dn{};
     dn.offsets = offsets; dn.E = c.E; dn.rows_sh = rows_sh;
     dn.N = c.d; dn.K = c.F; dn.N_sh = c.d; dn.K_sh = c.F_shared;
@@ -680,7 +679,7 @@ static int layer_forward_impl(const moe_cfg* cfg, const void* x, const void* Wr,
     cudaEvent_t const* ev = reinterpret_cast<cudaEvent_t const*>(events);
     if (ev) MOE_CUDA(cudaEventRecord(ev[0], st), "event record");
     const FrontSmallPlan fp = front_small_plan(c.T, c.d, c.E, c.k);
-    if (fp.ok && small_front_enabled()) {
+    if (fp.ok && small_front_enabled(c)) {
         // decode-sized batch: route + dispatch in one launch (the stage
         // events after it coincide: the dispatch stage reads as zero)
         FrontSmallArgs a{};
@@ -763,6 +762,18 @@ int moe_test_hold_lookback_block(void* ws, size_t ws_bytes, int block, void* str
     MOE_CUDA(cudaMemcpyAsync(at<int>(ws, 0) + kCtrlHoldBlock, &value, sizeof(int),
                              cudaMemcpyHostToDevice, (cudaStream_t)stream),
              "hold-block write");
+    return MOE_OK;
+}
+
+int moe_test_hold_gemm_stage(void* ws, size_t ws_bytes, int iteration, void* stream) {
+    if (!ws) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL%s");
+    if (ws_bytes < kCtrlWords * 4) return fail(MOE_ERR_WORKSPACE, "workspace too small%s");
+    if (iteration < 0) return fail(MOE_ERR_INVALID_ARG, "iteration must be >= 0%s");
+    static thread_local int value;      // pageable source; the copy is staged at enqueue
+    value = iteration + 1;
+    MOE_CUDA(cudaMemcpyAsync(at<int>(ws, 0) + kCtrlHoldGemm, &value, sizeof(int),
+                             cudaMemcpyHostToDevice, (cudaStream_t)stream),
+             "hold-stage write");
     return MOE_OK;
 }
 

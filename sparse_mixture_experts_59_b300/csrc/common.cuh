@@ -21,6 +21,7 @@ enum CtrlWord {
     kCtrlRouterDone = 3,
     kCtrlHoldBlock = 4,     // test hook: look-back block (id + 1) that never publishes
     kCtrlFrontDone = 5,     // decode-sized route + dispatch: CTAs done with phase 1
+    kCtrlHoldGemm = 6,      // test hook: up-projection ring iteration (+ 1) never loaded
     kCtrlWords = 64
 };
 

@@ -417,10 +417,12 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
         // ------------------------------------------------ TMA producer (weights)
         if (lane == 0) {
             int it = 0;
-            bool ok = true;
+            bool ok = true, held = false;
+            const int hold_it = p.hold ? *p.hold - 1 : -1;
             FOR_EACH_SEG(t)
                 for (int kb = t.kb0; ok && kb < t.kb1; ++kb)
                     for (int j = 0; j < t.nblk; ++j, ++it) {
+                        if (it == hold_it) { ok = false; held = true; break; }   // test hook
                         const int s = it % F::WSTAGES;
                         const uint32_t ph = (uint32_t)(it / F::WSTAGES) & 1u;
                         if (!ptx::mbar_wait_nap(&wempty[s], ph ^ 1u, s_abort, 64)) { ok = false; break; }
@@ -432,7 +434,7 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
                     }
                 if (!ok) break;
             }
-            if (!ok) {
+            if (!ok && !held) {
                 *s_abort = 1;
                 raise_error(p.status, MOE_ERR_DEVICE_TIMEOUT);
             }

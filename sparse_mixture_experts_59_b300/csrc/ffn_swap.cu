@@ -172,7 +172,8 @@ ffn_swap_kernel(const __grid_constant__ CUtensorMap mapW, const __grid_constant_
         // ------------------------------------------- TMA producer (both CTAs)
         if (lane == 0) {
             int it = 0;
-            bool ok = true;
+            bool ok = true, held = false;
+            const int hold_it = p.hold ? *p.hold - 1 : -1;
             for (int tile = cluster; ok && tile < total; tile += nclusters) {
                 const STile t = decode<MODE>(p, s_start, s_off, G, tile);
                 const CUtensorMap* mW = t.sh ? &mapW_sh : &mapW;
@@ -181,6 +182,7 @@ ffn_swap_kernel(const __grid_constant__ CUtensorMap mapW, const __grid_constant_
                 const int wrow = t.wbase + t.u0 + (int)rank * UNITS_CTA;
                 const int trow = t.tok0 + (int)rank * (t.nmma >> 1);
                 for (int kb = 0; kb < t.nk; ++kb, ++it) {
+                    if (it == hold_it) { ok = false; held = true; break; }   // test hook
                     const int s = it % STAGES;
                     const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
                     if (!ptx::mbar_wait(&empty[s], ph ^ 1u, s_abort)) { ok = false; break; }
@@ -195,7 +197,7 @@ ffn_swap_kernel(const __grid_constant__ CUtensorMap mapW, const __grid_constant_
                     ptx::tma_load_2d_pair(sB + s * B_BYTES, mX, fb, kb * BK, trow);
                 }
             }
-            if (!ok) {
+            if (!ok && !held) {
                 *s_abort = 1;
                 raise_error(p.status, MOE_ERR_DEVICE_TIMEOUT);
             }

@@ -124,13 +124,15 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
             int it = 0;
-            bool ok = true;
+            bool ok = true, held = false;
+            const int hold_it = p.hold ? *p.hold - 1 : -1;
             for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
                 const Tile t = tcffn::decode_tile<MODE, BM>(p, s_start, s_off, G, tile);
                 const CUtensorMap* mA = t.sh ? &mapA_sh : &mapA;
                 const CUtensorMap* mB0 = t.sh ? &mapB_sh : &mapB;
                 const CUtensorMap* mB1 = (MODE == kModeSwiglu) ? (t.sh ? &mapB2_sh : &mapB2) : mB0;
                 for (int kb = 0; kb < t.nk; ++kb, ++it) {
+                    if (it == hold_it) { ok = false; held = true; break; }   // test hook
                     const int s = it % STAGES;
                     const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
                     if (!ptx::mbar_wait(&empty[s], ph ^ 1u, s_abort)) { ok = false; break; }
@@ -140,7 +142,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
                     ptx::tma_load_2d(sB + s * B_BYTES + B_BYTES / 2, mB1, &full[s], kb * BK, t.wrow1);
                 }
             }
-            if (!ok) {
+            if (!ok && !held) {
                 *s_abort = 1;
                 raise_error(p.status, MOE_ERR_DEVICE_TIMEOUT);
             }

@@ -122,7 +122,8 @@ ffn_tc2_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
         // ------------------------------------------- TMA producer (both CTAs)
         if (lane == 0) {
             int it = 0;
-            bool ok = true;
+            bool ok = true, held = false;
+            const int hold_it = p.hold ? *p.hold - 1 : -1;
             for (int tile = cluster; ok && tile < total; tile += nclusters) {
                 const Tile t = tcffn::decode_tile<MODE, TILE_M>(p, s_start, s_off, G, tile);
                 const CUtensorMap* mA = t.sh ? &mapA_sh : &mapA;
@@ -134,6 +135,7 @@ ffn_tc2_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
                 const int arow = t.arow + (int)rank * HALF_M;
                 const int brow = leader ? t.wrow0 : t.wrow1;
                 for (int kb = 0; kb < t.nk; ++kb, ++it) {
+                    if (it == hold_it) { ok = false; held = true; break; }   // test hook
                     const int s = it % STAGES;
                     const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
                     if (!ptx::mbar_wait(&empty[s], ph ^ 1u, s_abort)) { ok = false; break; }
@@ -142,7 +144,7 @@ ffn_tc2_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
                     ptx::tma_load_2d_pair(sB + s * B_BYTES, mB, full_leader + 8u * s, kb * BK, brow);
                 }
             }
-            if (!ok) {
+            if (!ok && !held) {
                 *s_abort = 1;
                 raise_error(p.status, MOE_ERR_DEVICE_TIMEOUT);
             }

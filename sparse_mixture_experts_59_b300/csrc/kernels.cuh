@@ -143,6 +143,8 @@ struct TcFfnArgs {
     int split_tickets;        //   their number
     float* split_part;        //   fp32 partial sums
     long long split_bytes;    //   their capacity
+    const int* hold;          // test hook (up-projection launches): if *hold = n > 0, each
+                              //   CTA's weight producer stops before ring iteration n - 1
 };
 int ffn_tc_smem_bytes();
 // maps: A, B, B2, A_sh, B_sh, B2_sh (see ffn_tc.cu)

@@ -61,3 +61,35 @@ def test_kernel_launches_per_step(name, launches):
     """Decode-sized batches route and dispatch in one launch; larger ones in
     four.  Then gather, up, down, combine."""
     assert bench.kernels_per_step(workloads.config(name)) == launches
+
+
+def test_weight_bytes_of_the_decode_layers():
+    """Bytes streamed when all 8 Mixtral experts are hit: 3 bf16 matrices of
+    4096 x 14336 each (352 MB per expert); E4M3 codes are one byte each plus
+    fp32 row scales (2F + d per expert); packed 4-bit rows are 80 bytes per
+    128 values plus the same row scales."""
+    cfg = workloads.config("mixtral_decode")
+    d, F = cfg["d"], cfg["F"]
+    counts = [4] * 8
+    assert bench.weight_bytes(cfg, counts) == (8 * 3 * d * F * 2, 8)
+    c8 = dict(cfg, weight_fp8=True)
+    assert bench.weight_bytes(c8, counts)[0] == 8 * (3 * d * F + (2 * F + d) * 4)
+    c4 = dict(cfg, weight_fp4=True)
+    assert bench.weight_bytes(c4, counts)[0] == 8 * (3 * d * F // 128 * 80 + (2 * F + d) * 4)
+    # experts without kept rows stream nothing; the shared expert always streams
+    c3 = workloads.config("fine_grained")
+    got, hit = bench.weight_bytes(c3, [0, 3] + [0] * 254)
+    assert hit == 1 and got == 3 * 7168 * 2048 * 2 * 2
+    # fp32 GELU experts with biases
+    c0 = workloads.config("tiny_fp32")
+    assert bench.weight_bytes(c0, [1] * 8)[0] == 8 * (2 * 128 * 256 + 256 + 128) * 4
+
+
+def test_gemm_roofline_takes_the_slower_roof():
+    peaks = {"bf16_tflops": 1000.0, "hbm_gbs": 5000.0}
+    alg = {"up": 2e12, "down": 1e12}
+    r = bench.gemm_roofline(alg, 5e9, 4e-3, peaks)         # 3 ms of flop, 1 ms of bytes
+    assert r["bound"] == "tensor" and r["roofline_ms"] == pytest.approx(3.0)
+    assert r["frac"] == pytest.approx(0.75)
+    r = bench.gemm_roofline(alg, 25e9, 10e-3, peaks)       # 5 ms of bytes
+    assert r["bound"] == "hbm" and r["frac"] == pytest.approx(0.5)

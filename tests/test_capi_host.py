@@ -134,3 +134,22 @@ def test_dispatch_rejects_misaligned_prob_mean(lib):
     p[1] = ctypes.c_void_p(0x100000 + 0x1000 + 1)          # prob_mean
     rc = lib.moe_dispatch(ctypes.byref(c), *p[:9], ctypes.c_void_p(0x200000), ws_bytes, None)
     assert rc == 1 and "prob_mean" in lib.moe_last_error().decode()
+
+
+def test_config_kernel_choice_fields_are_validated(lib):
+    """gemm_kernel and route_path sit at the end of moe_cfg; out-of-range
+    values are refused by name (which also shows the binding's field layout
+    matches the header's)."""
+    base = workloads.config("mixtral_prefill", T=64, d=64, F=64, E=8, k=2)
+    for kern in ("auto", "tc1", "pair", "swap"):
+        assert binding.workspace_size(dict(base, gemm_kernel=kern)) > 0
+    c = binding.make_config(base)
+    c.gemm_kernel = 4
+    n = ctypes.c_size_t(0)
+    assert lib.moe_workspace_size(ctypes.byref(c), ctypes.byref(n)) == 1
+    assert "gemm_kernel" in lib.moe_last_error().decode()
+    c = binding.make_config(dict(base, route_path="separate"))
+    assert c.route_path == 1 and lib.moe_workspace_size(ctypes.byref(c), ctypes.byref(n)) == 0
+    c.route_path = 2
+    assert lib.moe_workspace_size(ctypes.byref(c), ctypes.byref(n)) == 1
+    assert "route_path" in lib.moe_last_error().decode()

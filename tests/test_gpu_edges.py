@@ -153,3 +153,36 @@ def test_lookback_wait_times_out_and_reports():
     ref = oracle.dispatch(idx.numpy(), 8, -1)
     np.testing.assert_array_equal(do["dest"].cpu().numpy(), ref["dest"])
     assert binding.device_status(ws) == 0
+
+
+@pytest.mark.parametrize("kern,low,hold", [("tc1", None, 0), ("tc1", None, 5), ("pair", None, 0),
+                                           ("pair", None, 5), ("swap", None, 0), ("swap", None, 5),
+                                           ("auto", "fp8", 0)])
+def test_gemm_wait_times_out_and_reports(kern, low, hold):
+    """Failure path of the expert GEMMs' bounded waits: with the up-projection's
+    weight producer stopped before ring iteration `hold` (the copy never
+    arrives), the MMA issuer (FP8: the converters) gives up after about a
+    second, the device status reads MOE_ERR_DEVICE_TIMEOUT, the kernel drains
+    its own copies and MMAs, frees its tensor memory and returns, and a clean
+    call on a fresh workspace reproduces the earlier output bit for bit.
+    d = 1024 gives every CTA with a tile 16 K blocks, so iteration 5 falls
+    inside the first tile (after loads and MMAs are in flight)."""
+    import time
+    cfg = workloads.config("mixtral_prefill", T=300, d=1024, F=384, E=4, k=2, seed=77,
+                           gemm_kernel=kern)
+    inp = workloads.make_inputs(cfg, device="cuda")
+    if low == "fp8":
+        inp = workloads.quantize_experts_fp8(inp)
+        cfg = inp["cfg"]
+    layer = binding.MoeLayer(cfg, inp)
+    ref = layer.forward(inp["x"])["y"].clone()
+    assert binding.device_status(layer.ws) == 0
+    binding.test_hold_gemm_stage(layer.ws, hold)
+    t0 = time.time()
+    layer.forward(inp["x"])
+    assert binding.device_status(layer.ws) == 5        # MOE_ERR_DEVICE_TIMEOUT
+    assert time.time() - t0 < 60
+    layer.ws = binding.new_workspace(layer.c)
+    y = layer.forward(inp["x"])["y"]
+    assert binding.device_status(layer.ws) == 0
+    assert torch.equal(y, ref)

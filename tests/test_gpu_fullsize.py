@@ -1,8 +1,12 @@
 """GPU parity at the full workload sizes, in the launch configuration the bench
 times.  Integer outputs (routing, counts, permutation, drops) are compared in
-full; the aux loss in full; router logits and layer outputs on sampled tokens,
-which the oracle computes one by one from copies of just the experts those
-tokens use."""
+full; the aux loss in full; router logits on sampled tokens; layer outputs on
+a stratified sample of tokens that reaches every tile the expert GEMMs
+compute: for every expert segment its first and last row and a row in each
+128-row tile (the token tiles of every GEMM kernel are 128 rows or multiples
+of them, and each sampled token's output covers all output columns), plus
+fully dropped tokens where there are any.  The oracle computes the sampled
+tokens one by one from copies of just the experts they use."""
 import numpy as np
 import pytest
 import torch
@@ -13,7 +17,8 @@ from sparse_mixture_experts_59_b300 import binding, workloads
 
 pytestmark = pytest.mark.gpu
 WANT = ("logits", "topk_idx", "topk_w", "counts_pre", "counts_kept", "drop_mask", "stats")
-SAMPLES = {"mixtral_prefill": 12, "mixtral_decode": 32, "fine_grained": 4, "switch_skewed": 24}
+TILE_ROWS = 128
+DROPPED_SAMPLES = 8
 
 
 def _subset_inputs(inp, cfg, tokens, idx, drop):
@@ -38,7 +43,8 @@ def _subset_inputs(inp, cfg, tokens, idx, drop):
     return sub, sidx, sdrop
 
 
-@pytest.fixture(scope="module", params=list(SAMPLES))
+@pytest.fixture(scope="module", params=["mixtral_prefill", "mixtral_decode", "fine_grained",
+                                                "switch_skewed"])
 def full(request):
     name = request.param
     cfg = workloads.config(name)
@@ -92,23 +98,48 @@ def test_full_size_sampled_logits(full):
     np.testing.assert_array_equal(g["topk_idx"].numpy()[tokens][clear], idx_own[clear])
 
 
-def test_full_size_sampled_layer_output(full):
+def stratified_tokens(disp, T, k, tile=TILE_ROWS):
+    """Tokens whose kept rows include, for every expert segment [offsets[e],
+    offsets[e+1]) of the permuted rows, its first row, its last row and at
+    least one row of each `tile`-row tile.  Greedy: a cell not yet covered by
+    an earlier token's rows takes the token of its middle row (or of the named
+    row)."""
+    offs, perm, dest = disp["offsets"], disp["perm_src"], disp["dest"]
+    cells = []
+    for e in range(len(offs) - 1):
+        a, b = int(offs[e]), int(offs[e + 1])
+        if b == a:
+            continue
+        cells += [(a, a + 1), (b - 1, b)]
+        cells += [(r0, min(b, r0 + tile)) for r0 in range(a, b, tile)]
+    covered = np.zeros(int(offs[-1]), bool)
+    chosen = []
+    for lo, hi in cells:
+        if covered[lo:hi].any():
+            continue
+        t = int(perm[(lo + hi - 1) // 2]) // k
+        chosen.append(t)
+        rows = dest[t * k:(t + 1) * k]
+        covered[rows[rows >= 0]] = True
+    assert all(covered[lo:hi].any() for lo, hi in cells)
+    return sorted(set(chosen))
+
+
+def test_full_size_layer_output_on_every_tile(full):
     cfg, g, inp, out = full["cfg"], full["gpu"], full["inp"], full["out"]
-    T, k = cfg["T"], cfg["k"]
+    T, E, k = cfg["T"], cfg["E"], cfg["k"]
     idx = g["topk_idx"].numpy()
     drop = g["drop_mask"].numpy()
-    n = SAMPLES[full["name"]]
-    rng = np.random.default_rng(12)
-    if n >= T:
-        tokens = list(range(T))
-    else:
-        full_drop = drop.reshape(T, k).all(axis=1)
-        kept_t = np.nonzero(~full_drop)[0]
-        drop_t = np.nonzero(full_drop)[0]
-        nk = min(len(kept_t), n if len(drop_t) == 0 else (n + 1) // 2)
-        nd = min(len(drop_t), n - nk)
-        tokens = sorted(rng.choice(kept_t, nk, replace=False).tolist() +
-                        (rng.choice(drop_t, nd, replace=False).tolist() if nd else []))
+    disp = oracle.dispatch(idx, E, oracle.capacity(T, k, E, cfg["capacity_factor"]))
+    tokens = stratified_tokens(disp, T, k)
+    full_drop = np.nonzero(drop.reshape(T, k).all(axis=1))[0]
+    if len(full_drop):
+        rng = np.random.default_rng(12)
+        extra = rng.choice(full_drop, min(DROPPED_SAMPLES, len(full_drop)), replace=False)
+        tokens = sorted(set(tokens) | set(int(t) for t in extra))
+    # every expert with kept rows is reached
+    reached = {int(idx[t, s]) for t in tokens for s in range(k) if not drop[t * k + s]}
+    assert reached == {e for e in range(E) if disp["counts_kept"][e] > 0}
     sub, sidx, sdrop = _subset_inputs(inp, cfg, tokens, idx, drop)
     w = f64(g["topk_w"])[tokens]
     ref = oracle.layer_tokens(sub, sidx, w, sdrop, np.arange(len(tokens)))["y"]

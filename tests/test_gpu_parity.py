@@ -1,8 +1,6 @@
 """GPU parity of the whole path against the CPU oracle, element by element, on
 scaled-down copies of each workload (sizes that span several tiles and leave
 ragged row, column and reduction tails).  Calls go through the C ABI."""
-import os
-
 import numpy as np
 import pytest
 import torch
@@ -29,20 +27,12 @@ def _params():
 @pytest.fixture(scope="module", params=_params())
 def run(request):
     name, _, kern = request.param.partition("@")
-    old = os.environ.get("MOE_GEMM_KERNEL")
-    if kern:
-        os.environ["MOE_GEMM_KERNEL"] = kern
-    try:
-        yield _run(name)
-    finally:
-        if old is None:
-            os.environ.pop("MOE_GEMM_KERNEL", None)
-        else:
-            os.environ["MOE_GEMM_KERNEL"] = old
+    return _run(name, kern or "auto")
 
 
-def _run(name):
+def _run(name, kern="auto"):
     cfg = small_cfg(name)
+    cfg["gemm_kernel"] = kern
     inp_cpu = workloads.make_inputs(cfg, device="cpu")
     inp = workloads.to_device(inp_cpu, "cuda")
     layer = binding.MoeLayer(cfg, inp)
