@@ -444,6 +444,9 @@ def run_sustained(layer, x, outputs, cfg, alg, args, world, peaks, peak_src, loc
     one = max(time.perf_counter() - probe, 1e-4)
     n = int(min(5000, max(50, args.sustained_seconds / one)))
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(n)]
+    for row in evs:                 # torch creates the CUDA event at its first record
+        for e in row:
+            e.record()
     clocks = ClockSampler(local)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
