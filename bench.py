@@ -155,56 +155,87 @@ _REASON_BITS = (("gpu_idle", 0x1), ("sw_power_cap", 0x4), ("hw_slowdown", 0x8),
                 ("hw_power_brake_slowdown", 0x80))
 
 
+class _Nvml:
+    """Read-only NVML queries through ctypes (libnvidia-ml ships with the
+    driver; the Python wrapper may be absent): SM clock, its maximum, power
+    draw and the active clock-event reasons of one device."""
+    NVML_CLOCK_SM = 1
+
+    def __init__(self, cuda_index):
+        import ctypes
+        self.ct = ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit_v2 failed")
+        self.lib = lib
+        self.dev = ctypes.c_void_p()
+        uuid = str(torch.cuda.get_device_properties(cuda_index).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        if lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.dev)) != 0:
+            if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(cuda_index), ctypes.byref(self.dev)) != 0:
+                raise RuntimeError("no NVML handle for the device")
+        self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def _uint(self, fn, *args):
+        v = self.ct.c_uint(0)
+        if fn(self.dev, *args, self.ct.byref(v)) != 0:
+            raise RuntimeError("NVML query failed")
+        return v.value
+
+    def sm_mhz(self):
+        return self._uint(self.lib.nvmlDeviceGetClockInfo, self.ct.c_int(self.NVML_CLOCK_SM))
+
+    def sm_max_mhz(self):
+        return self._uint(self.lib.nvmlDeviceGetMaxClockInfo, self.ct.c_int(self.NVML_CLOCK_SM))
+
+    def power_w(self):
+        return self._uint(self.lib.nvmlDeviceGetPowerUsage) / 1000.0
+
+    def reasons(self):
+        v = self.ct.c_ulonglong(0)
+        if self.reasons_fn(self.dev, self.ct.byref(v)) != 0:
+            raise RuntimeError("NVML reasons query failed")
+        return v.value
+
+
 class ClockSampler:
     """SM clock, power and clock-event reasons of one GPU, sampled about every
-    2 ms by NVML in a background thread while a timed region runs (a timed
-    region of 20 layer calls lasts ~40 ms, so a 100 ms nvidia-smi poll would
-    mostly see the idle GPU around it).  Without NVML the summary is None.
-    The summary's sm_mhz is the median over samples taken while the GPU was
-    busy (NVML's gpu_idle reason clear)."""
+    2 ms through NVML in a background thread while a timed region runs (a
+    timed region of 20 layer calls lasts ~40 ms, so a 100 ms nvidia-smi poll
+    would mostly see the idle GPU around it).  The summary's sm_mhz is the
+    median over samples taken while the GPU was busy (NVML's gpu_idle reason
+    clear); without NVML the summary only says why."""
 
     def __init__(self, device_index, period_s=0.002):
         self.idx = device_index
         self.period = period_s
         self.rows = []
         self.thread = None
-        self.handle = None
-        self.nvml = None
-
-    def _handle(self):
-        import pynvml
-        pynvml.nvmlInit()
-        self.nvml = pynvml
-        try:
-            uuid = str(torch.cuda.get_device_properties(self.idx).uuid)
-            return pynvml.nvmlDeviceGetHandleByUUID(("GPU-" + uuid) if not uuid.startswith("GPU-") else uuid)
-        except Exception:
-            return pynvml.nvmlDeviceGetHandleByIndex(self.idx)
+        self.error = None
 
     def start(self):
         import threading
         self.rows = []
+        self.error = None
         try:
-            self.handle = self._handle()
-        except Exception:
-            self.handle = None
+            self.nv = _Nvml(self.idx)
+            self.max_mhz = float(self.nv.sm_max_mhz())
+        except Exception as e:          # no NVML: the summary says why
+            self.error = "NVML unavailable: %s" % e
             return
-        nv = self.nvml
-        get_reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
-            nv.nvmlDeviceGetCurrentClocksThrottleReasons
-        self.max_mhz = float(nv.nvmlDeviceGetMaxClockInfo(self.handle, nv.NVML_CLOCK_SM))
         self.stop_flag = threading.Event()
 
         def loop():
             n = 0
             while not self.stop_flag.is_set():
                 try:
-                    sm = nv.nvmlDeviceGetClockInfo(self.handle, nv.NVML_CLOCK_SM)
-                    rs = get_reasons(self.handle)
-                    pw = nv.nvmlDeviceGetPowerUsage(self.handle) / 1000.0 if n % 4 == 0 else None
+                    sm = self.nv.sm_mhz()
+                    rs = self.nv.reasons()
+                    pw = self.nv.power_w() if n % 4 == 0 else None
                     self.rows.append((time.perf_counter(), float(sm), int(rs), pw))
-                except Exception:
-                    pass
+                except Exception as e:
+                    self.error = "NVML query failed: %s" % e
                 n += 1
                 time.sleep(self.period)
 
@@ -213,13 +244,13 @@ class ClockSampler:
 
     def stop(self):
         if self.thread is None:
-            return None
+            return {"error": self.error} if self.error else None
         self.stop_flag.set()
         self.thread.join(timeout=5)
         self.thread = None
         rows = self.rows
         if not rows:
-            return None
+            return {"error": self.error or "no samples"}
         busy = [r for r in rows if not (r[2] & 0x1)]
         use = busy if busy else rows
         sm = np.array([r[1] for r in use])
@@ -232,7 +263,8 @@ class ClockSampler:
         return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": self.max_mhz,
                 "sm_mhz_p10": float(np.percentile(sm, 10)), "sm_mhz_p90": float(np.percentile(sm, 90)),
                 "reasons": sorted(reasons), "samples": len(rows), "samples_busy": len(busy),
-                "power_w_max": float(max(power)) if power else None, "source": "nvml, ~2 ms period"}
+                "power_w_max": float(max(power)) if power else None,
+                "source": "NVML (ctypes), ~2 ms period"}
 
 
 # ------------------------------------------------------------ our path
@@ -247,11 +279,15 @@ def algorithmic(cfg, R):
     return dict(up=up, down=down, router=router, total=up + down + router)
 
 
-def time_layer(layer, x, steps, warmup, world, outputs, clocks=None):
+def time_layer(layer, x, steps, warmup, world, outputs, clocks=None, settle_s=1.0):
     """Times `steps` plain layer calls (the step time), then the same number of
     calls that record CUDA events at every stage boundary on the launching
     stream (the per-kernel times: events between kernels can keep a kernel
-    from starting early, so they stay out of the step time)."""
+    from starting early, so they stay out of the step time).  Each pass starts
+    after `settle_s` of idle GPU: under the 1.1 kW cap a B300 running these
+    GEMMs back to back lowers its SM clock after about 40 ms, so two passes
+    timed one after the other would see different clocks; with the pause both
+    see the same state (the sustained leg measures the capped state)."""
     for _ in range(warmup):
         layer.forward(x, outputs=outputs)
     torch.cuda.synchronize()
@@ -260,6 +296,7 @@ def time_layer(layer, x, steps, warmup, world, outputs, clocks=None):
         raise RuntimeError("device status %d after warm-up" % st)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
+    time.sleep(settle_s)            # both passes start from an idle GPU (see docstring)
     barrier(world)
     torch.cuda.synchronize()
     if clocks:
@@ -276,6 +313,8 @@ def time_layer(layer, x, steps, warmup, world, outputs, clocks=None):
         for e in row:
             e.record()
     pstart, pend = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    time.sleep(settle_s)
     torch.cuda.synchronize()
     pstart.record()
     for i in range(steps):
@@ -443,6 +482,7 @@ def run_sustained(layer, x, outputs, cfg, alg, args, world, peaks, peak_src, loc
     torch.cuda.synchronize()
     one = max(time.perf_counter() - probe, 1e-4)
     n = int(min(5000, max(50, args.sustained_seconds / one)))
+    time.sleep(1.0)                 # start from an idle GPU, like the timed passes
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(n)]
     for row in evs:                 # torch creates the CUDA event at its first record
         for e in row:
