@@ -450,34 +450,44 @@ int run_expert_ffn(const moe_cfg& c, const DevInfo& di, const void* x, const int
     dn.status = status;
     CUtensorMap maps[6];
     if (gk == kGemmRing) {
-        // maps: W, W3, X (token rows, small boxes), W_sh, W3_sh, X_sh
+        // maps: W, W3, W_sh, W3_sh, X (boxes of 128, 64, 32, 16 rows), X_sh (same)
+        CUtensorMap rm[12];
+        auto token_maps = [&](CUtensorMap* out, const void* base, uint64_t rows, int K,
+                              const char* what) {
+            for (int b = 0; b < 4; ++b) {
+                const int rc = encode_rows(&out[b], base, rows, (uint64_t)K, what, 128u >> b);
+                if (rc != MOE_OK) return rc;
+            }
+            return (int)MOE_OK;
+        };
         const uint32_t wb_up = (uint32_t)ffn_ring_weight_box_rows(up_mode);
-        const uint32_t tb = (uint32_t)ffn_ring_token_box_rows();
-        MOE_TRY(encode_rows(&maps[0], w.W1, (uint64_t)c.E * c.F, c.d, "W1", wb_up));
-        MOE_TRY(encode_rows(&maps[1], c.act == MOE_SWIGLU ? w.W3 : w.W1, (uint64_t)c.E * c.F, c.d,
+        MOE_TRY(encode_rows(&rm[0], w.W1, (uint64_t)c.E * c.F, c.d, "W1", wb_up));
+        MOE_TRY(encode_rows(&rm[1], c.act == MOE_SWIGLU ? w.W3 : w.W1, (uint64_t)c.E * c.F, c.d,
                             "W3", wb_up));
-        MOE_TRY(encode_rows(&maps[2], Xp, (uint64_t)A, c.d, "gathered rows", tb));
+        MOE_TRY(token_maps(&rm[4], Xp, (uint64_t)A, c.d, "gathered rows"));
         if (rows_sh) {
-            MOE_TRY(encode_rows(&maps[3], w.S1, (uint64_t)c.F_shared, c.d, "S1", wb_up));
-            MOE_TRY(encode_rows(&maps[4], w.S3, (uint64_t)c.F_shared, c.d, "S3", wb_up));
-            MOE_TRY(encode_rows(&maps[5], x, (uint64_t)c.T, c.d, "x", tb));
+            MOE_TRY(encode_rows(&rm[2], w.S1, (uint64_t)c.F_shared, c.d, "S1", wb_up));
+            MOE_TRY(encode_rows(&rm[3], w.S3, (uint64_t)c.F_shared, c.d, "S3", wb_up));
+            MOE_TRY(token_maps(&rm[8], x, (uint64_t)c.T, c.d, "x"));
         } else {
-            maps[3] = maps[0]; maps[4] = maps[1]; maps[5] = maps[2];
+            rm[2] = rm[0]; rm[3] = rm[1];
+            for (int b = 0; b < 4; ++b) rm[8 + b] = rm[4 + b];
         }
-        MOE_CUDA(launch_ffn_ring(up_mode, maps, up, st), "up-projection launch");
+        MOE_CUDA(launch_ffn_ring(up_mode, rm, up, st), "up-projection launch");
         if (ev) MOE_CUDA(cudaEventRecord(ev[1], st), "event record");
         const uint32_t wb_dn = (uint32_t)ffn_ring_weight_box_rows(kModeDown);
-        MOE_TRY(encode_rows(&maps[0], w.W2, (uint64_t)c.E * c.d, c.F, "W2", wb_dn));
-        maps[1] = maps[0];
-        MOE_TRY(encode_rows(&maps[2], H, (uint64_t)A, c.F, "hidden rows", tb));
+        MOE_TRY(encode_rows(&rm[0], w.W2, (uint64_t)c.E * c.d, c.F, "W2", wb_dn));
+        rm[1] = rm[0];
+        MOE_TRY(token_maps(&rm[4], H, (uint64_t)A, c.F, "hidden rows"));
         if (rows_sh) {
-            MOE_TRY(encode_rows(&maps[3], w.S2, (uint64_t)c.d, c.F_shared, "S2", wb_dn));
-            maps[4] = maps[3];
-            MOE_TRY(encode_rows(&maps[5], Hsh, (uint64_t)c.T, c.F_shared, "shared hidden rows", tb));
+            MOE_TRY(encode_rows(&rm[2], w.S2, (uint64_t)c.d, c.F_shared, "S2", wb_dn));
+            rm[3] = rm[2];
+            MOE_TRY(token_maps(&rm[8], Hsh, (uint64_t)c.T, c.F_shared, "shared hidden rows"));
         } else {
-            maps[3] = maps[0]; maps[4] = maps[1]; maps[5] = maps[2];
+            rm[2] = rm[0]; rm[3] = rm[1];
+            for (int b = 0; b < 4; ++b) rm[8 + b] = rm[4 + b];
         }
-        MOE_CUDA(launch_ffn_ring(kModeDown, maps, dn, st), "down-projection launch");
+        MOE_CUDA(launch_ffn_ring(kModeDown, rm, dn, st), "down-projection launch");
         if (ev) MOE_CUDA(cudaEventRecord(ev[2], st), "event record");
         return MOE_OK;
     }

@@ -28,8 +28,9 @@
 //
 // Roles (192 threads per CTA):
 //   warp 0      TMA producer (both CTAs): this CTA's 128 weight rows and its
-//               half of each MMA's tokens (16-row boxes) into a 5-deep ring of
-//               36 KB stages; both CTAs signal the leader's full barrier
+//               half of each MMA's tokens (boxes of 128/64/32/16 rows) into a
+//               5-deep ring of 36 KB stages; both CTAs signal the leader's full
+//               barrier; weight boxes are also prefetched into L2 ahead of it
 //   warp 1      TMEM allocation (512 columns, pair); MMA issuer (leader only)
 //   warps 2-5   epilogue (both CTAs): 32 tokens at a time from TMEM, staged as
 //               [token][unit] in shared memory, written with 16-byte stores
@@ -53,7 +54,8 @@ constexpr int CHUNK = 32;                    // TMEM columns per ring chunk
 constexpr int NCHUNK = 16;                   // 512 columns
 constexpr int PIECE_MAX = 8;                 // chunks per MMA (N <= 256)
 constexpr int NSLOT = 4;                     // tiles in flight between issuer and epilogue
-constexpr int TOK_BOX = 16;                  // token rows per TMA box
+constexpr int TOK_BOX = 16;                  // smallest token box (rows)
+constexpr int PF_DIST = 16;                  // weight k-blocks prefetched into L2 ahead of the ring
 constexpr int A_BYTES = 128 * BK * 2;        // this CTA's 128 weight rows
 constexpr int B_BYTES = HALF_MAX * BK * 2;   // up to 160 token rows
 constexpr int TMEM_COLS = 512;
@@ -153,12 +155,21 @@ __device__ __forceinline__ Pieces ring_pieces(int pos, int nch) {
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
+// Tensor maps of one launch: weights (boxes of ffn_ring_weight_box_rows rows)
+// and token rows with boxes of 128, 64, 32 and 16 rows, so that any piece
+// half (a multiple of 16 rows up to 128) loads in at most three copies.
+struct RingMaps {
+    CUtensorMap w, w3, w_sh, w3_sh;
+    CUtensorMap x[4], x_sh[4];
+};
+
 template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-ffn_ring_kernel(const __grid_constant__ CUtensorMap mapW, const __grid_constant__ CUtensorMap mapW3,
-                const __grid_constant__ CUtensorMap mapX, const __grid_constant__ CUtensorMap mapW_sh,
-                const __grid_constant__ CUtensorMap mapW3_sh,
-                const __grid_constant__ CUtensorMap mapX_sh, const TcFfnArgs p) {
+ffn_ring_kernel(const __grid_constant__ RingMaps maps, const TcFfnArgs p) {
+    const CUtensorMap& mapW = maps.w;
+    const CUtensorMap& mapW3 = maps.w3;
+    const CUtensorMap& mapW_sh = maps.w_sh;
+    const CUtensorMap& mapW3_sh = maps.w3_sh;
     constexpr int UNITS_CTA = RingTraits<MODE>::UNITS_CTA;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -202,7 +213,7 @@ ffn_ring_kernel(const __grid_constant__ CUtensorMap mapW, const __grid_constant_
         ptx::fence_mbarrier_init();
         ptx::prefetch_tensormap(&mapW);
         ptx::prefetch_tensormap(&mapW3);
-        ptx::prefetch_tensormap(&mapX);
+        for (int i = 0; i < 4; ++i) ptx::prefetch_tensormap(&maps.x[i]);
     }
     if (warp == 1) {
         ptx::tmem_alloc_pair(s_tmem, TMEM_COLS);
@@ -232,13 +243,32 @@ ffn_ring_kernel(const __grid_constant__ CUtensorMap mapW, const __grid_constant_
             int it = 0, pos = 0;
             bool ok = true, held = false;
             const int hold_it = p.hold ? *p.hold - 1 : -1;
+            // L2 prefetch cursor for this CTA's weight rows, PF_DIST k-blocks
+            // ahead of the loads and across tile boundaries: every weight byte
+            // is read once, from DRAM, and the shared-memory ring alone holds
+            // too few bytes in flight to keep HBM busy
+            int pf_tile = cluster, pf_kb = 0;
+            RTile pft{};
+            if (pf_tile < total) pft = decode<MODE>(p, s_start, s_off, G, pf_tile);
+            auto pf_step = [&]() {
+                if (pf_tile >= total) return;
+                const int wr = pft.wbase + pft.u0 + (int)rank * UNITS_CTA;
+                ptx::tma_prefetch_2d(pft.sh ? &mapW_sh : &mapW, pf_kb * BK, wr);
+                if (MODE == kModeSwiglu) ptx::tma_prefetch_2d(pft.sh ? &mapW3_sh : &mapW3, pf_kb * BK, wr);
+                if (++pf_kb == pft.nk) {
+                    pf_kb = 0;
+                    pf_tile += nclusters;
+                    if (pf_tile < total) pft = decode<MODE>(p, s_start, s_off, G, pf_tile);
+                }
+            };
+            for (int i = 0; i < PF_DIST; ++i) pf_step();
             for (int tile = cluster; ok && tile < total; tile += nclusters) {
                 const RTile t = decode<MODE>(p, s_start, s_off, G, tile);
                 const Pieces pc = ring_pieces(pos, t.nch);
                 pos = (pos + t.nch) % NCHUNK;
                 const CUtensorMap* mW = t.sh ? &mapW_sh : &mapW;
                 const CUtensorMap* mW3 = t.sh ? &mapW3_sh : &mapW3;
-                const CUtensorMap* mX = t.sh ? &mapX_sh : &mapX;
+                const CUtensorMap* mX = t.sh ? maps.x_sh : maps.x;   // boxes of 128, 64, 32, 16 rows
                 const int wrow = t.wbase + t.u0 + (int)rank * UNITS_CTA;
                 // both CTAs' bytes land on the leader's barrier
                 const uint32_t tx = 2u * (uint32_t)(A_BYTES + t.nch * (CHUNK / 2) * BK * 2);
@@ -261,14 +291,22 @@ ffn_ring_kernel(const __grid_constant__ CUtensorMap mapW, const __grid_constant_
 #pragma unroll
                     for (int j = 0; j < 3; ++j) {
                         if (j < pc.n) {
-                            const int h = pc.len[j] * (CHUNK / 2);
+                            const int h = pc.len[j] * (CHUNK / 2);   // 16..128 rows
                             const int src = t.tok0 + tp + (int)rank * h;
                             uint8_t* dst = sB + s * B_BYTES + (tp / 2) * (BK * 2);
-                            for (int i = 0; i < h; i += TOK_BOX)
-                                ptx::tma_load_2d_pair(dst + i * (BK * 2), mX, fb, kb * BK, src + i);
+                            int r = 0;
+#pragma unroll
+                            for (int b = 0; b < 4; ++b) {
+                                const int rows = 128 >> b;
+                                if (h == 128 ? b == 0 : (b > 0 && (h & rows))) {
+                                    ptx::tma_load_2d_pair(dst + r * (BK * 2), &mX[b], fb, kb * BK, src + r);
+                                    r += rows;
+                                }
+                            }
                             tp += pc.len[j] * CHUNK;
                         }
                     }
+                    pf_step();
                 }
             }
             if (!ok && !held) {
@@ -462,8 +500,14 @@ ffn_ring_kernel(const __grid_constant__ CUtensorMap mapW, const __grid_constant_
 }
 
 template <int MODE>
-cudaError_t launch_mode(const CUtensorMap* maps, const TcFfnArgs& p, cudaStream_t st) {
+cudaError_t launch_mode(const CUtensorMap* m, const TcFfnArgs& p, cudaStream_t st) {
     auto kernel = ffn_ring_kernel<MODE>;
+    RingMaps maps;
+    maps.w = m[0]; maps.w3 = m[1]; maps.w_sh = m[2]; maps.w3_sh = m[3];
+    for (int i = 0; i < 4; ++i) {
+        maps.x[i] = m[4 + i];
+        maps.x_sh[i] = m[8 + i];
+    }
     cudaError_t err =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (err != cudaSuccess) return err;
@@ -489,14 +533,12 @@ cudaError_t launch_mode(const CUtensorMap* maps, const TcFfnArgs& p, cudaStream_
         if (clusters < 1) return cudaErrorInvalidConfiguration;
         if (dev >= 0 && dev < 64) cached[dev] = clusters;
     }
-    return launch_kernel(kernel, dim3(2 * clusters), dim3(NUM_THREADS), SMEM_BYTES, st, 2, maps[0],
-                         maps[1], maps[2], maps[3], maps[4], maps[5], p);
+    return launch_kernel(kernel, dim3(2 * clusters), dim3(NUM_THREADS), SMEM_BYTES, st, 2, maps, p);
 }
 
 }  // namespace
 
 int ffn_ring_weight_box_rows(int mode) { return mode == kModeSwiglu ? 64 : 128; }
-int ffn_ring_token_box_rows() { return TOK_BOX; }
 
 cudaError_t launch_ffn_ring(int mode, const CUtensorMap* maps, const TcFfnArgs& p, cudaStream_t st) {
     if (mode == kModeSwiglu) return launch_mode<kModeSwiglu>(maps, p, st);
