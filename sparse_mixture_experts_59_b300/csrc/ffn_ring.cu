@@ -26,17 +26,19 @@
 // are rounded up to a multiple of 32; the extra rows are computed on whatever
 // the tile reads (next segment, or TMA's zero fill) and never stored.
 //
-// Roles (192 threads per CTA):
+// Roles (224 threads per CTA):
 //   warp 0      TMA producer (both CTAs): this CTA's 128 weight rows and its
 //               half of each MMA's tokens (boxes of 128/64/32/16 rows) into a
 //               5-deep ring of 36 KB stages; both CTAs signal the leader's full
 //               barrier; weight boxes are also prefetched into L2 ahead of it
-//   warp 1      TMEM allocation (512 columns, pair); MMA issuer (leader only)
+//   warp 1      TMEM allocation (512 columns, pair); MMA issuer 0 (leader only)
 //   warps 2-5   epilogue (both CTAs): 32 tokens at a time from TMEM, staged as
 //               [token][unit] in shared memory, written with 16-byte stores
-// Barriers: full/empty per stage; tfull/slot_free per tile slot (at most NSLOT
-// tiles between issuer and epilogue); chunk_free per TMEM chunk (8 arrivals:
-// the four epilogue warps of both CTAs).  Every wait is bounded.
+//   warp 6      MMA issuer 1 (leader only): the second piece of each tile
+// Barriers: full/empty per stage (empty: one commit per issuer); tfull (one
+// commit per issuer) and slot_free per tile slot (at most NSLOT tiles between
+// the issuers and the epilogue); chunk_free per TMEM chunk (8 arrivals: the
+// four epilogue warps of both CTAs).  Every wait is bounded.
 #include "common.cuh"
 #include "kernels.cuh"
 #include "launch.cuh"
@@ -59,8 +61,10 @@ constexpr int PF_DIST = 16;                  // weight k-blocks prefetched into 
 constexpr int A_BYTES = 128 * BK * 2;        // this CTA's 128 weight rows
 constexpr int B_BYTES = HALF_MAX * BK * 2;   // up to 160 token rows
 constexpr int TMEM_COLS = 512;
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS = 224;             // 7 warps: producer, issuer 0, 4 epilogue, issuer 1
 constexpr int EPI_THREADS = 128;
+constexpr int NISS = 2;                      // MMA-issuing threads
+constexpr int ISSUER2_WARP = 6;
 constexpr uint16_t BOTH = 0x3;
 constexpr uint16_t LEADER_ONLY = 0x1;
 constexpr uint32_t CHUNK_ARRIVALS = 8;       // 4 epilogue warps x 2 CTAs
@@ -75,7 +79,7 @@ constexpr int OFF_OUT = OFF_XCH + 64 * XCH_LD * 4;
 constexpr int OFF_TOKA = OFF_OUT + 32 * OUT_LD * 2;
 constexpr int OFF_TOKW = OFF_TOKA + TOK_MAX * 4;
 constexpr int OFF_BAR = OFF_TOKW + TOK_MAX * 4;
-constexpr int NUM_BARS = 2 * STAGES + 2 * NSLOT + NCHUNK + 1;
+constexpr int NUM_BARS = 2 * STAGES + 2 * NSLOT + NCHUNK + NISS;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int OFF_START = OFF_MISC + 16;
 constexpr int OFF_OFFS = OFF_START + (kMaxExperts + 2) * 4;
@@ -201,14 +205,14 @@ ffn_ring_kernel(const __grid_constant__ RingMaps maps, const TcFfnArgs p) {
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(&full[s], 1);
-            ptx::mbar_init(&empty[s], 1);
+            ptx::mbar_init(&empty[s], NISS);
         }
         for (int a = 0; a < NSLOT; ++a) {
-            ptx::mbar_init(&tfull[a], 1);
+            ptx::mbar_init(&tfull[a], NISS);
             ptx::mbar_init(&slot_free[a], CHUNK_ARRIVALS);
         }
         for (int c = 0; c < NCHUNK; ++c) ptx::mbar_init(&chunk_free[c], CHUNK_ARRIVALS);
-        ptx::mbar_init(drain, 1);
+        for (int i = 0; i < NISS; ++i) ptx::mbar_init(&drain[i], 1);
         *s_abort = 0;
         ptx::fence_mbarrier_init();
         ptx::prefetch_tensormap(&mapW);
@@ -317,8 +321,15 @@ ffn_ring_kernel(const __grid_constant__ RingMaps maps, const TcFfnArgs p) {
                 for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
                     ptx::mbar_wait(&full[j % STAGES], (uint32_t)(j / STAGES) & 1u, nullptr);
         }
-    } else if (warp == 1) {
-        // ----------------------------------------- MMA issuer (leader only)
+    } else if (warp == 1 || warp == ISSUER2_WARP) {
+        // ------------------------------------ MMA issuers (leader only, two)
+        // A single thread issues a tcgen05.mma only every ~150 cycles in this
+        // pipeline, about the tensor time of one N = 256 MMA, so the pieces of
+        // a tile are issued from two threads on different schedulers: issuer 0
+        // (warp 1) takes pieces 0 and 2, issuer 1 (warp 6) piece 1.  Both walk
+        // every stage (the empty and accumulator-full barriers count two
+        // commits), and each waits only for the TMEM chunks of its own pieces.
+        const int me = (warp == 1) ? 0 : 1;
         if (leader && lane == 0) {
             int it = 0, tc = 0, pos = 0;
             uint32_t cpar = 0;            // bit c: parity of the next use of chunk c
@@ -331,10 +342,20 @@ ffn_ring_kernel(const __grid_constant__ RingMaps maps, const TcFfnArgs p) {
                     ok = false;
                     break;
                 }
-                for (int j = 0; ok && j < t.nch; ++j) {     // the tile's chunks are drained
-                    const int c = (pos + j) % NCHUNK;
-                    if (!ptx::mbar_wait(&chunk_free[c], ((cpar >> c) & 1u) ^ 1u, s_abort)) ok = false;
-                    cpar ^= 1u << c;
+                bool mine[3];
+#pragma unroll
+                for (int j = 0; j < 3; ++j) mine[j] = j < pc.n && ((j == 1) == (me == 1));
+                for (int j = 0; ok && j < 3; ++j) {         // own pieces' chunks are drained
+                    if (j >= pc.n) break;
+                    for (int i = 0; i < pc.len[j]; ++i) {
+                        const int c = pc.c[j] + i;
+                        if (mine[j] &&
+                            !ptx::mbar_wait(&chunk_free[c], ((cpar >> c) & 1u) ^ 1u, s_abort)) {
+                            ok = false;
+                            break;
+                        }
+                        cpar ^= 1u << c;
+                    }
                 }
                 if (!ok) break;
                 pos = (pos + t.nch) % NCHUNK;
@@ -359,7 +380,7 @@ ffn_ring_kernel(const __grid_constant__ RingMaps maps, const TcFfnArgs p) {
                     for (int kk = 0; kk < BK / 16; ++kk) {
 #pragma unroll
                         for (int j = 0; j < 3; ++j) {
-                            if (j < pc.n) {
+                            if (mine[j]) {
                                 const uint64_t bd = ptx::sw128_desc(b0 + boff[j]);
                                 ptx::mma_bf16_pair(tmem_base + dcol[j], ad + (uint64_t)(kk * 2),
                                                    bd + (uint64_t)(kk * 2), idesc[j],
@@ -376,10 +397,10 @@ ffn_ring_kernel(const __grid_constant__ RingMaps maps, const TcFfnArgs p) {
                 *s_abort = 1;
                 raise_error(p.status, MOE_ERR_DEVICE_TIMEOUT);
             }
-            ptx::mma_commit_pair_mc(drain, LEADER_ONLY);
-            ptx::mbar_wait(drain, 0, nullptr);
+            ptx::mma_commit_pair_mc(&drain[me], LEADER_ONLY);
+            ptx::mbar_wait(&drain[me], 0, nullptr);
         }
-    } else {
+    } else if (warp >= 2 && warp < 6) {
         // ------------------------------------------- epilogue (both CTAs)
         const int q = warp & 3;                  // TMEM lane quadrant = weight rows q*32..
         const int et = threadIdx.x - 64;         // 0..127 among the epilogue threads
