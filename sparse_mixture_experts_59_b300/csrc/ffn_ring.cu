@@ -27,18 +27,17 @@
 // the tile reads (next segment, or TMA's zero fill) and never stored.
 //
 // Roles (224 threads per CTA):
-//   warp 0      TMA producer (both CTAs): this CTA's 128 weight rows and its
-//               half of each MMA's tokens (boxes of 128/64/32/16 rows) into a
-//               5-deep ring of 36 KB stages; both CTAs signal the leader's full
-//               barrier; weight boxes are also prefetched into L2 ahead of it
-//   warp 1      TMEM allocation (512 columns, pair); MMA issuer 0 (leader only)
+//   warp 0      weight producer (both CTAs): this CTA's 128 weight rows of each
+//               stage of a 5-deep ring of 36 KB stages
+//   warp 6      token producer (both CTAs): this CTA's half of each MMA's token
+//               rows (boxes of 128/64/32/16 rows) into the same stages
+//   warp 1      TMEM allocation (512 columns, pair); MMA issuer (leader only)
 //   warps 2-5   epilogue (both CTAs): 32 tokens at a time from TMEM, staged as
 //               [token][unit] in shared memory, written with 16-byte stores
-//   warp 6      MMA issuer 1 (leader only): the second piece of each tile
-// Barriers: full/empty per stage (empty: one commit per issuer); tfull (one
-// commit per issuer) and slot_free per tile slot (at most NSLOT tiles between
-// the issuers and the epilogue); chunk_free per TMEM chunk (8 arrivals: the
-// four epilogue warps of both CTAs).  Every wait is bounded.
+// Barriers: weight-full, token-full (the leader's: both CTAs' bytes) and empty
+// per stage; tfull/slot_free per tile slot (at most NSLOT
+// tiles between issuer and epilogue); chunk_free per TMEM chunk (8 arrivals:
+// the four epilogue warps of both CTAs).  Every wait is bounded.
 #include "common.cuh"
 #include "kernels.cuh"
 #include "launch.cuh"
@@ -57,14 +56,12 @@ constexpr int NCHUNK = 16;                   // 512 columns
 constexpr int PIECE_MAX = 8;                 // chunks per MMA (N <= 256)
 constexpr int NSLOT = 4;                     // tiles in flight between issuer and epilogue
 constexpr int TOK_BOX = 16;                  // smallest token box (rows)
-constexpr int PF_DIST = 16;                  // weight k-blocks prefetched into L2 ahead of the ring
 constexpr int A_BYTES = 128 * BK * 2;        // this CTA's 128 weight rows
 constexpr int B_BYTES = HALF_MAX * BK * 2;   // up to 160 token rows
 constexpr int TMEM_COLS = 512;
-constexpr int NUM_THREADS = 224;             // 7 warps: producer, issuer 0, 4 epilogue, issuer 1
+constexpr int NUM_THREADS = 224;             // 7 warps: weight producer, issuer, 4 epilogue, token producer
 constexpr int EPI_THREADS = 128;
-constexpr int NISS = 2;                      // MMA-issuing threads
-constexpr int ISSUER2_WARP = 6;
+constexpr int TOKP_WARP = 6;
 constexpr uint16_t BOTH = 0x3;
 constexpr uint16_t LEADER_ONLY = 0x1;
 constexpr uint32_t CHUNK_ARRIVALS = 8;       // 4 epilogue warps x 2 CTAs
@@ -79,7 +76,7 @@ constexpr int OFF_OUT = OFF_XCH + 64 * XCH_LD * 4;
 constexpr int OFF_TOKA = OFF_OUT + 32 * OUT_LD * 2;
 constexpr int OFF_TOKW = OFF_TOKA + TOK_MAX * 4;
 constexpr int OFF_BAR = OFF_TOKW + TOK_MAX * 4;
-constexpr int NUM_BARS = 2 * STAGES + 2 * NSLOT + NCHUNK + NISS;
+constexpr int NUM_BARS = 3 * STAGES + 2 * NSLOT + NCHUNK + 1;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int OFF_START = OFF_MISC + 16;
 constexpr int OFF_OFFS = OFF_START + (kMaxExperts + 2) * 4;
@@ -185,9 +182,10 @@ ffn_ring_kernel(const __grid_constant__ RingMaps maps, const TcFfnArgs p) {
     int* s_tok_a = reinterpret_cast<int*>(smem + OFF_TOKA);
     float* s_tok_w = reinterpret_cast<float*>(smem + OFF_TOKW);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-    uint64_t* full = bars;
-    uint64_t* empty = bars + STAGES;
-    uint64_t* tfull = bars + 2 * STAGES;
+    uint64_t* wfull = bars;                  // weight rows of a stage landed
+    uint64_t* kfull = bars + STAGES;         // token rows of a stage landed
+    uint64_t* empty = bars + 2 * STAGES;
+    uint64_t* tfull = bars + 3 * STAGES;
     uint64_t* slot_free = tfull + NSLOT;
     uint64_t* chunk_free = slot_free + NSLOT;
     uint64_t* drain = chunk_free + NCHUNK;
@@ -204,15 +202,16 @@ ffn_ring_kernel(const __grid_constant__ RingMaps maps, const TcFfnArgs p) {
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            ptx::mbar_init(&full[s], 1);
-            ptx::mbar_init(&empty[s], NISS);
+            ptx::mbar_init(&wfull[s], 1);
+            ptx::mbar_init(&kfull[s], 1);
+            ptx::mbar_init(&empty[s], 1);
         }
         for (int a = 0; a < NSLOT; ++a) {
-            ptx::mbar_init(&tfull[a], NISS);
+            ptx::mbar_init(&tfull[a], 1);
             ptx::mbar_init(&slot_free[a], CHUNK_ARRIVALS);
         }
         for (int c = 0; c < NCHUNK; ++c) ptx::mbar_init(&chunk_free[c], CHUNK_ARRIVALS);
-        for (int i = 0; i < NISS; ++i) ptx::mbar_init(&drain[i], 1);
+        ptx::mbar_init(drain, 1);
         *s_abort = 0;
         ptx::fence_mbarrier_init();
         ptx::prefetch_tensormap(&mapW);
@@ -237,35 +236,25 @@ ffn_ring_kernel(const __grid_constant__ RingMaps maps, const TcFfnArgs p) {
     const uint32_t tmem_base = *s_tmem;
     const int G = p.E + (p.rows_sh > 0 ? 1 : 0);
     const int total = s_start[G];
-    const uint32_t full_leader = ptx::mapa_shared(ptx::smem_u32(full), 0);
+    const uint32_t wfull_leader = ptx::mapa_shared(ptx::smem_u32(wfull), 0);
+    const uint32_t kfull_leader = ptx::mapa_shared(ptx::smem_u32(kfull), 0);
     const uint32_t slot_free_leader = ptx::mapa_shared(ptx::smem_u32(slot_free), 0);
     const uint32_t chunk_free_leader = ptx::mapa_shared(ptx::smem_u32(chunk_free), 0);
 
-    if (warp == 0) {
-        // ------------------------------------------- TMA producer (both CTAs)
+    if (warp == 0 || warp == TOKP_WARP) {
+        // ---------------------- TMA producers (both CTAs): weights / tokens
+        // Issuing a bulk-tensor copy keeps its thread busy ~150 cycles here,
+        // and a stage takes two weight copies plus one to three token copies,
+        // more than one thread can issue in the ~600 cycles of MMA work per
+        // stage.  So warp 0 loads the weight rows and warp 6 the token rows,
+        // each on its own full barrier of the stage (both CTAs' bytes land on
+        // the leader's barriers).
+        const bool wprod = (warp == 0);
         if (lane == 0) {
             int it = 0, pos = 0;
             bool ok = true, held = false;
-            const int hold_it = p.hold ? *p.hold - 1 : -1;
-            // L2 prefetch cursor for this CTA's weight rows, PF_DIST k-blocks
-            // ahead of the loads and across tile boundaries: every weight byte
-            // is read once, from DRAM, and the shared-memory ring alone holds
-            // too few bytes in flight to keep HBM busy
-            int pf_tile = cluster, pf_kb = 0;
-            RTile pft{};
-            if (pf_tile < total) pft = decode<MODE>(p, s_start, s_off, G, pf_tile);
-            auto pf_step = [&]() {
-                if (pf_tile >= total) return;
-                const int wr = pft.wbase + pft.u0 + (int)rank * UNITS_CTA;
-                ptx::tma_prefetch_2d(pft.sh ? &mapW_sh : &mapW, pf_kb * BK, wr);
-                if (MODE == kModeSwiglu) ptx::tma_prefetch_2d(pft.sh ? &mapW3_sh : &mapW3, pf_kb * BK, wr);
-                if (++pf_kb == pft.nk) {
-                    pf_kb = 0;
-                    pf_tile += nclusters;
-                    if (pf_tile < total) pft = decode<MODE>(p, s_start, s_off, G, pf_tile);
-                }
-            };
-            for (int i = 0; i < PF_DIST; ++i) pf_step();
+            const int hold_it = (wprod && p.hold) ? *p.hold - 1 : -1;
+            const uint32_t fbase = wprod ? wfull_leader : kfull_leader;
             for (int tile = cluster; ok && tile < total; tile += nclusters) {
                 const RTile t = decode<MODE>(p, s_start, s_off, G, tile);
                 const Pieces pc = ring_pieces(pos, t.nch);
@@ -274,20 +263,23 @@ ffn_ring_kernel(const __grid_constant__ RingMaps maps, const TcFfnArgs p) {
                 const CUtensorMap* mW3 = t.sh ? &mapW3_sh : &mapW3;
                 const CUtensorMap* mX = t.sh ? maps.x_sh : maps.x;   // boxes of 128, 64, 32, 16 rows
                 const int wrow = t.wbase + t.u0 + (int)rank * UNITS_CTA;
-                // both CTAs' bytes land on the leader's barrier
-                const uint32_t tx = 2u * (uint32_t)(A_BYTES + t.nch * (CHUNK / 2) * BK * 2);
+                const uint32_t tx = wprod ? 2u * (uint32_t)A_BYTES
+                                          : 2u * (uint32_t)(t.nch * (CHUNK / 2) * BK * 2);
                 for (int kb = 0; kb < t.nk; ++kb, ++it) {
                     if (it == hold_it) { ok = false; held = true; break; }   // test hook
                     const int s = it % STAGES;
                     const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
                     if (!ptx::mbar_wait(&empty[s], ph ^ 1u, s_abort)) { ok = false; break; }
-                    if (leader) ptx::mbar_arrive_expect_tx(&full[s], tx);
-                    const uint32_t fb = full_leader + 8u * s;
-                    if (MODE == kModeSwiglu) {   // 64 gate rows, then the 64 matching up rows
-                        ptx::tma_load_2d_pair(sA + s * A_BYTES, mW, fb, kb * BK, wrow);
-                        ptx::tma_load_2d_pair(sA + s * A_BYTES + A_BYTES / 2, mW3, fb, kb * BK, wrow);
-                    } else {
-                        ptx::tma_load_2d_pair(sA + s * A_BYTES, mW, fb, kb * BK, wrow);
+                    if (leader) ptx::mbar_arrive_expect_tx(wprod ? &wfull[s] : &kfull[s], tx);
+                    const uint32_t fb = fbase + 8u * s;
+                    if (wprod) {
+                        if (MODE == kModeSwiglu) {   // 64 gate rows, then the 64 matching up rows
+                            ptx::tma_load_2d_pair(sA + s * A_BYTES, mW, fb, kb * BK, wrow);
+                            ptx::tma_load_2d_pair(sA + s * A_BYTES + A_BYTES / 2, mW3, fb, kb * BK, wrow);
+                        } else {
+                            ptx::tma_load_2d_pair(sA + s * A_BYTES, mW, fb, kb * BK, wrow);
+                        }
+                        continue;
                     }
                     // piece j: this CTA holds its half of the piece's tokens, at
                     // shared-memory row (first token of the piece) / 2
@@ -310,26 +302,20 @@ ffn_ring_kernel(const __grid_constant__ RingMaps maps, const TcFfnArgs p) {
                             tp += pc.len[j] * CHUNK;
                         }
                     }
-                    pf_step();
                 }
             }
             if (!ok && !held) {
                 *s_abort = 1;
                 raise_error(p.status, MOE_ERR_DEVICE_TIMEOUT);
             }
+            // the leader's barriers count both CTAs' bytes: let them land
             if (leader)
                 for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
-                    ptx::mbar_wait(&full[j % STAGES], (uint32_t)(j / STAGES) & 1u, nullptr);
+                    ptx::mbar_wait(wprod ? &wfull[j % STAGES] : &kfull[j % STAGES],
+                                   (uint32_t)(j / STAGES) & 1u, nullptr);
         }
-    } else if (warp == 1 || warp == ISSUER2_WARP) {
-        // ------------------------------------ MMA issuers (leader only, two)
-        // A single thread issues a tcgen05.mma only every ~150 cycles in this
-        // pipeline, about the tensor time of one N = 256 MMA, so the pieces of
-        // a tile are issued from two threads on different schedulers: issuer 0
-        // (warp 1) takes pieces 0 and 2, issuer 1 (warp 6) piece 1.  Both walk
-        // every stage (the empty and accumulator-full barriers count two
-        // commits), and each waits only for the TMEM chunks of its own pieces.
-        const int me = (warp == 1) ? 0 : 1;
+    } else if (warp == 1) {
+        // ----------------------------------------- MMA issuer (leader only)
         if (leader && lane == 0) {
             int it = 0, tc = 0, pos = 0;
             uint32_t cpar = 0;            // bit c: parity of the next use of chunk c
@@ -342,20 +328,10 @@ ffn_ring_kernel(const __grid_constant__ RingMaps maps, const TcFfnArgs p) {
                     ok = false;
                     break;
                 }
-                bool mine[3];
-#pragma unroll
-                for (int j = 0; j < 3; ++j) mine[j] = j < pc.n && ((j == 1) == (me == 1));
-                for (int j = 0; ok && j < 3; ++j) {         // own pieces' chunks are drained
-                    if (j >= pc.n) break;
-                    for (int i = 0; i < pc.len[j]; ++i) {
-                        const int c = pc.c[j] + i;
-                        if (mine[j] &&
-                            !ptx::mbar_wait(&chunk_free[c], ((cpar >> c) & 1u) ^ 1u, s_abort)) {
-                            ok = false;
-                            break;
-                        }
-                        cpar ^= 1u << c;
-                    }
+                for (int j = 0; ok && j < t.nch; ++j) {     // the tile's chunks are drained
+                    const int c = (pos + j) % NCHUNK;
+                    if (!ptx::mbar_wait(&chunk_free[c], ((cpar >> c) & 1u) ^ 1u, s_abort)) ok = false;
+                    cpar ^= 1u << c;
                 }
                 if (!ok) break;
                 pos = (pos + t.nch) % NCHUNK;
@@ -372,7 +348,11 @@ ffn_ring_kernel(const __grid_constant__ RingMaps maps, const TcFfnArgs p) {
                 for (int kb = 0; kb < t.nk; ++kb, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
-                    if (!ptx::mbar_wait(&full[s], ph, s_abort)) { ok = false; break; }
+                    if (!ptx::mbar_wait(&wfull[s], ph, s_abort) ||
+                        !ptx::mbar_wait(&kfull[s], ph, s_abort)) {
+                        ok = false;
+                        break;
+                    }
                     ptx::tc_fence_after();
                     const uint64_t ad = ptx::sw128_desc(ptx::smem_u32(sA + s * A_BYTES));
                     const uint32_t b0 = ptx::smem_u32(sB + s * B_BYTES);
@@ -380,7 +360,7 @@ ffn_ring_kernel(const __grid_constant__ RingMaps maps, const TcFfnArgs p) {
                     for (int kk = 0; kk < BK / 16; ++kk) {
 #pragma unroll
                         for (int j = 0; j < 3; ++j) {
-                            if (mine[j]) {
+                            if (j < pc.n) {
                                 const uint64_t bd = ptx::sw128_desc(b0 + boff[j]);
                                 ptx::mma_bf16_pair(tmem_base + dcol[j], ad + (uint64_t)(kk * 2),
                                                    bd + (uint64_t)(kk * 2), idesc[j],
@@ -397,8 +377,8 @@ ffn_ring_kernel(const __grid_constant__ RingMaps maps, const TcFfnArgs p) {
                 *s_abort = 1;
                 raise_error(p.status, MOE_ERR_DEVICE_TIMEOUT);
             }
-            ptx::mma_commit_pair_mc(&drain[me], LEADER_ONLY);
-            ptx::mbar_wait(&drain[me], 0, nullptr);
+            ptx::mma_commit_pair_mc(drain, LEADER_ONLY);
+            ptx::mbar_wait(drain, 0, nullptr);
         }
     } else if (warp >= 2 && warp < 6) {
         // ------------------------------------------- epilogue (both CTAs)
