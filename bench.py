@@ -213,6 +213,12 @@ class ClockSampler:
         self.rows = []
         self.thread = None
         self.error = None
+        self.windows = []
+
+    def mark(self, t0, t1):
+        """A host-time window [t0, t1] (time.perf_counter) that covered GPU
+        work: the summary uses only samples taken inside such windows."""
+        self.windows.append((t0, t1))
 
     def start(self):
         import threading
@@ -251,6 +257,10 @@ class ClockSampler:
         rows = self.rows
         if not rows:
             return {"error": self.error or "no samples"}
+        if self.windows:
+            rows = [r for r in rows if any(a <= r[0] <= b for a, b in self.windows)]
+            if not rows:
+                return {"error": "no samples inside the timed windows"}
         busy = [r for r in rows if not (r[2] & 0x1)]
         use = busy if busy else rows
         sm = np.array([r[1] for r in use])
@@ -262,9 +272,9 @@ class ClockSampler:
         power = [r[3] for r in rows if r[3] is not None]
         return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": self.max_mhz,
                 "sm_mhz_p10": float(np.percentile(sm, 10)), "sm_mhz_p90": float(np.percentile(sm, 90)),
-                "reasons": sorted(reasons), "samples": len(rows), "samples_busy": len(busy),
+                "reasons": sorted(reasons), "samples": len(rows),
                 "power_w_max": float(max(power)) if power else None,
-                "source": "NVML (ctypes), ~2 ms period"}
+                "source": "NVML (ctypes), ~2 ms period, samples inside the timed passes only"}
 
 
 # ------------------------------------------------------------ our path
@@ -301,11 +311,14 @@ def time_layer(layer, x, steps, warmup, world, outputs, clocks=None, settle_s=1.
     torch.cuda.synchronize()
     if clocks:
         clocks.start()
+    h0 = time.perf_counter()
     start.record()
     for _ in range(steps):
         layer.forward(x, outputs=outputs)
     end.record()
     torch.cuda.synchronize()
+    if clocks:
+        clocks.mark(h0, time.perf_counter())
     ms = start.elapsed_time(end) / steps
     # profiled pass: stage boundaries
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(steps)]
@@ -316,11 +329,14 @@ def time_layer(layer, x, steps, warmup, world, outputs, clocks=None, settle_s=1.
     torch.cuda.synchronize()
     time.sleep(settle_s)
     torch.cuda.synchronize()
+    h0 = time.perf_counter()
     pstart.record()
     for i in range(steps):
         layer.forward(x, outputs=outputs, events=evs[i])
     pend.record()
     torch.cuda.synchronize()
+    if clocks:
+        clocks.mark(h0, time.perf_counter())
     clk = clocks.stop() if clocks else None
     barrier(world)
     torch.cuda.synchronize()
@@ -492,11 +508,13 @@ def run_sustained(layer, x, outputs, cfg, alg, args, world, peaks, peak_src, loc
     torch.cuda.synchronize()
     barrier(world)
     clocks.start()
+    h0 = time.perf_counter()
     start.record()
     for i in range(n):
         layer.forward(x, outputs=outputs, events=evs[i])
     end.record()
     torch.cuda.synchronize()
+    clocks.mark(h0, time.perf_counter())
     clk = clocks.stop()
     if binding.device_status(layer.ws) != 0:
         raise RuntimeError("device status after the sustained loop")
