@@ -1,7 +1,7 @@
 // ffn_ring.cu -- bf16 grouped expert GEMMs for layers with many short expert
 // segments (a few hundred rows each, e.g. 256 routed experts with top-8):
 // weights on the MMA's M, tokens on N, on CTA pairs (tcgen05 cta_group::2),
-// one token tile for a whole segment of up to 320 rows, accumulators taken
+// one token tile for a whole segment of up to 288 rows, accumulators taken
 // from a ring of tensor-memory columns.
 //
 // Same maths and fused epilogues as ffn_swap.cu (see ffn_tc.cu for the pages'
@@ -11,9 +11,9 @@
 // A tcgen05 MMA takes time in proportion to N, and the weight tile of a pair
 // (256 rows x K) costs the same to stream whatever N is.  So a segment is best
 // covered by a single token tile: every weight byte then feeds all of the
-// segment's tokens.  With ~256 +- 16 rows per segment that needs N up to ~320,
+// segment's tokens.  With ~256 +- 16 rows per segment that needs N up to ~288,
 // above one MMA's 256: a tile is issued as up to three MMAs of <= 256 columns
-// over the same weight stage.  Two 320-column accumulators do not fit in the
+// over the same weight stage.  Two 288-column accumulators do not fit in the
 // 512 columns of TMEM, so instead of two fixed accumulators the columns form a
 // ring of 16 chunks of 32: tile i takes the next ceil(n_i / 32) chunks (its
 // MMAs split where the ring wraps), the epilogue frees each chunk as soon as it
@@ -21,21 +21,21 @@
 // free -- usually while the epilogue is still draining tile i.
 //
 // Per pair tile: 256 weight rows (128 per CTA; SwiGLU: 64 gate + the 64
-// matching up rows per CTA) x up to 320 tokens.  Segments longer than 320
-// rows are cut into ceil(rows / 320) tiles of equal size (+-1).  Token counts
+// matching up rows per CTA) x up to 288 tokens.  Segments longer than 288
+// rows are cut into ceil(rows / 288) tiles of equal size (+-1).  Token counts
 // are rounded up to a multiple of 32; the extra rows are computed on whatever
 // the tile reads (next segment, or TMA's zero fill) and never stored.
 //
 // Roles (224 threads per CTA):
 //   warp 0      weight producer (both CTAs): this CTA's 128 weight rows of each
-//               stage of a 5-deep ring of 36 KB stages
+//               K block into an 8-deep ring of 16 KB stages
 //   warp 6      token producer (both CTAs): this CTA's half of each MMA's token
-//               rows (boxes of 128/64/32/16 rows) into the same stages
+//               rows (boxes of 128/64/32/16 rows) into a 4-deep ring
 //   warp 1      TMEM allocation (512 columns, pair); MMA issuer (leader only)
 //   warps 2-5   epilogue (both CTAs): 32 tokens at a time from TMEM, staged as
 //               [token][unit] in shared memory, written with 16-byte stores
-// Barriers: weight-full, token-full (the leader's: both CTAs' bytes) and empty
-// per stage; tfull/slot_free per tile slot (at most NSLOT
+// Barriers: full (the leader's: both CTAs' bytes) and empty per stage of each
+// ring; tfull/slot_free per tile slot (at most NSLOT
 // tiles between issuer and epilogue); chunk_free per TMEM chunk (8 arrivals:
 // the four epilogue warps of both CTAs).  Every wait is bounded.
 #include "common.cuh"
@@ -48,8 +48,13 @@ namespace moe {
 namespace {
 
 constexpr int BK = 64;
-constexpr int STAGES = 5;
-constexpr int TOK_MAX = 320;                 // tokens per tile
+// Weight and token rows sit in two rings of their own depth.  Every weight
+// byte is read by one SM only and comes from DRAM (~3 us away under load), so
+// each SM needs ~128 KB of weight loads in flight to keep HBM busy; the token
+// rows are shared by the tiles of a segment and mostly hit L2.
+constexpr int WSTAGES = 8;                   // 16 KB weight stages
+constexpr int KSTAGES = 4;                   // up to 18 KB token stages
+constexpr int TOK_MAX = 288;                 // tokens per tile
 constexpr int HALF_MAX = TOK_MAX / 2;        // token rows per CTA
 constexpr int CHUNK = 32;                    // TMEM columns per ring chunk
 constexpr int NCHUNK = 16;                   // 512 columns
@@ -57,7 +62,7 @@ constexpr int PIECE_MAX = 8;                 // chunks per MMA (N <= 256)
 constexpr int NSLOT = 4;                     // tiles in flight between issuer and epilogue
 constexpr int TOK_BOX = 16;                  // smallest token box (rows)
 constexpr int A_BYTES = 128 * BK * 2;        // this CTA's 128 weight rows
-constexpr int B_BYTES = HALF_MAX * BK * 2;   // up to 160 token rows
+constexpr int B_BYTES = HALF_MAX * BK * 2;   // up to 144 token rows
 constexpr int TMEM_COLS = 512;
 constexpr int NUM_THREADS = 224;             // 7 warps: weight producer, issuer, 4 epilogue, token producer
 constexpr int EPI_THREADS = 128;
@@ -70,13 +75,13 @@ constexpr int XCH_LD = 33;                   // [64 units][33] fp32: up values, 
 constexpr int OUT_LD = 136;                  // [32 tokens][136] bf16: staged output rows
 
 constexpr int OFF_A = 0;
-constexpr int OFF_B = STAGES * A_BYTES;
-constexpr int OFF_XCH = OFF_B + STAGES * B_BYTES;
+constexpr int OFF_B = WSTAGES * A_BYTES;
+constexpr int OFF_XCH = OFF_B + KSTAGES * B_BYTES;
 constexpr int OFF_OUT = OFF_XCH + 64 * XCH_LD * 4;
 constexpr int OFF_TOKA = OFF_OUT + 32 * OUT_LD * 2;
 constexpr int OFF_TOKW = OFF_TOKA + TOK_MAX * 4;
 constexpr int OFF_BAR = OFF_TOKW + TOK_MAX * 4;
-constexpr int NUM_BARS = 3 * STAGES + 2 * NSLOT + NCHUNK + 1;
+constexpr int NUM_BARS = 2 * WSTAGES + 2 * KSTAGES + 2 * NSLOT + NCHUNK + 1;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int OFF_START = OFF_MISC + 16;
 constexpr int OFF_OFFS = OFF_START + (kMaxExperts + 2) * 4;
@@ -182,10 +187,11 @@ ffn_ring_kernel(const __grid_constant__ RingMaps maps, const TcFfnArgs p) {
     int* s_tok_a = reinterpret_cast<int*>(smem + OFF_TOKA);
     float* s_tok_w = reinterpret_cast<float*>(smem + OFF_TOKW);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-    uint64_t* wfull = bars;                  // weight rows of a stage landed
-    uint64_t* kfull = bars + STAGES;         // token rows of a stage landed
-    uint64_t* empty = bars + 2 * STAGES;
-    uint64_t* tfull = bars + 3 * STAGES;
+    uint64_t* wfull = bars;                  // weight stage landed
+    uint64_t* wempty = wfull + WSTAGES;      // weight stage consumed by the MMAs
+    uint64_t* kfull = wempty + WSTAGES;      // token stage landed
+    uint64_t* kempty = kfull + KSTAGES;      // token stage consumed
+    uint64_t* tfull = kempty + KSTAGES;
     uint64_t* slot_free = tfull + NSLOT;
     uint64_t* chunk_free = slot_free + NSLOT;
     uint64_t* drain = chunk_free + NCHUNK;
@@ -201,10 +207,13 @@ ffn_ring_kernel(const __grid_constant__ RingMaps maps, const TcFfnArgs p) {
     const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < WSTAGES; ++s) {
             ptx::mbar_init(&wfull[s], 1);
+            ptx::mbar_init(&wempty[s], 1);
+        }
+        for (int s = 0; s < KSTAGES; ++s) {
             ptx::mbar_init(&kfull[s], 1);
-            ptx::mbar_init(&empty[s], 1);
+            ptx::mbar_init(&kempty[s], 1);
         }
         for (int a = 0; a < NSLOT; ++a) {
             ptx::mbar_init(&tfull[a], 1);
@@ -250,6 +259,7 @@ ffn_ring_kernel(const __grid_constant__ RingMaps maps, const TcFfnArgs p) {
         // each on its own full barrier of the stage (both CTAs' bytes land on
         // the leader's barriers).
         const bool wprod = (warp == 0);
+        const int NST = wprod ? WSTAGES : KSTAGES;
         if (lane == 0) {
             int it = 0, pos = 0;
             bool ok = true, held = false;
@@ -267,9 +277,12 @@ ffn_ring_kernel(const __grid_constant__ RingMaps maps, const TcFfnArgs p) {
                                           : 2u * (uint32_t)(t.nch * (CHUNK / 2) * BK * 2);
                 for (int kb = 0; kb < t.nk; ++kb, ++it) {
                     if (it == hold_it) { ok = false; held = true; break; }   // test hook
-                    const int s = it % STAGES;
-                    const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
-                    if (!ptx::mbar_wait(&empty[s], ph ^ 1u, s_abort)) { ok = false; break; }
+                    const int s = it % NST;
+                    const uint32_t ph = (uint32_t)(it / NST) & 1u;
+                    if (!ptx::mbar_wait(wprod ? &wempty[s] : &kempty[s], ph ^ 1u, s_abort)) {
+                        ok = false;
+                        break;
+                    }
                     if (leader) ptx::mbar_arrive_expect_tx(wprod ? &wfull[s] : &kfull[s], tx);
                     const uint32_t fb = fbase + 8u * s;
                     if (wprod) {
@@ -310,9 +323,9 @@ ffn_ring_kernel(const __grid_constant__ RingMaps maps, const TcFfnArgs p) {
             }
             // the leader's barriers count both CTAs' bytes: let them land
             if (leader)
-                for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
-                    ptx::mbar_wait(wprod ? &wfull[j % STAGES] : &kfull[j % STAGES],
-                                   (uint32_t)(j / STAGES) & 1u, nullptr);
+                for (int j = (it > NST ? it - NST : 0); j < it; ++j)
+                    ptx::mbar_wait(wprod ? &wfull[j % NST] : &kfull[j % NST],
+                                   (uint32_t)(j / NST) & 1u, nullptr);
         }
     } else if (warp == 1) {
         // ----------------------------------------- MMA issuer (leader only)
@@ -346,16 +359,15 @@ ffn_ring_kernel(const __grid_constant__ RingMaps maps, const TcFfnArgs p) {
                     tp += len * CHUNK;
                 }
                 for (int kb = 0; kb < t.nk; ++kb, ++it) {
-                    const int s = it % STAGES;
-                    const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
-                    if (!ptx::mbar_wait(&wfull[s], ph, s_abort) ||
-                        !ptx::mbar_wait(&kfull[s], ph, s_abort)) {
+                    const int ws = it % WSTAGES, ks = it % KSTAGES;
+                    if (!ptx::mbar_wait(&wfull[ws], (uint32_t)(it / WSTAGES) & 1u, s_abort) ||
+                        !ptx::mbar_wait(&kfull[ks], (uint32_t)(it / KSTAGES) & 1u, s_abort)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
-                    const uint64_t ad = ptx::sw128_desc(ptx::smem_u32(sA + s * A_BYTES));
-                    const uint32_t b0 = ptx::smem_u32(sB + s * B_BYTES);
+                    const uint64_t ad = ptx::sw128_desc(ptx::smem_u32(sA + ws * A_BYTES));
+                    const uint32_t b0 = ptx::smem_u32(sB + ks * B_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
 #pragma unroll
@@ -368,7 +380,8 @@ ffn_ring_kernel(const __grid_constant__ RingMaps maps, const TcFfnArgs p) {
                             }
                         }
                     }
-                    ptx::mma_commit_pair_mc(&empty[s], BOTH);
+                    ptx::mma_commit_pair_mc(&wempty[ws], BOTH);
+                    ptx::mma_commit_pair_mc(&kempty[ks], BOTH);
                 }
                 if (!ok) break;
                 ptx::mma_commit_pair_mc(&tfull[slot], BOTH);
