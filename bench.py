@@ -54,7 +54,7 @@ def parse_args():
     ap.add_argument("--experts", type=int, default=None, help="override E (profiling cases)")
     ap.add_argument("--no-pdl", action="store_true",
                     help="launch without programmatic dependent launch (MOE_PDL=0)")
-    ap.add_argument("--gemm", default=None, choices=["tc1", "pair", "swap", "ring"],
+    ap.add_argument("--gemm", default=None, choices=["tc1", "pair", "swap"],
                     help="force the expert GEMM kernel (default: the library's choice)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -785,7 +785,7 @@ def run_sweep(args, world, local):
         inp["x"] = workloads.make_x(cfg, dev)
         inp["cfg"] = cfg
         entry = {"T": T}
-        for g in ("auto", "tc1", "swap", "pair", "ring"):
+        for g in ("auto", "tc1", "swap", "pair"):
             cfg = dict(base, T=T, gemm_kernel=g)
             layer = binding.MoeLayer(cfg, inp, device=dev)
             outputs = {"y": torch.empty_like(inp["x"]),

@@ -71,9 +71,7 @@ enum moe_status {
 enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 };
 enum moe_act { MOE_GELU_ERF = 0, MOE_SWIGLU = 1 };
 enum moe_scoring { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 };
-enum moe_gemm_kernel {
-    MOE_GEMM_AUTO = 0, MOE_GEMM_TC1 = 1, MOE_GEMM_PAIR = 2, MOE_GEMM_SWAP = 3, MOE_GEMM_RING = 4
-};
+enum moe_gemm_kernel { MOE_GEMM_AUTO = 0, MOE_GEMM_TC1 = 1, MOE_GEMM_PAIR = 2, MOE_GEMM_SWAP = 3 };
 enum moe_route_path { MOE_ROUTE_AUTO = 0, MOE_ROUTE_SEPARATE = 1 };
 
 /* Layer shape and options.
@@ -113,9 +111,8 @@ enum moe_route_path { MOE_ROUTE_AUTO = 0, MOE_ROUTE_SEPARATE = 1 };
  *  gemm_kernel  bf16 expert GEMM kernel: MOE_GEMM_AUTO (default) picks one from
  *           the shape; MOE_GEMM_TC1 (tokens on the MMA's M, 128-row tiles, one
  *           SM per tile), MOE_GEMM_PAIR (tokens on M, 256-row tiles on SM
- *           pairs), MOE_GEMM_SWAP (weights on M, tokens on N in tiles of up to
- *           256, SM pairs) or MOE_GEMM_RING (weights on M, one token tile of up
- *           to 320 rows per expert segment, SM pairs) forces one.  All give results within the bf16 tolerance of each other;
+ *           pairs) or MOE_GEMM_SWAP (weights on M, tokens on N in tiles of up
+ *           to 256, SM pairs) forces one.  All give results within the bf16 tolerance of each other;
  *           ignored by fp32 and low-bit layers.
  *  route_path MOE_ROUTE_AUTO (default): decode-sized batches (T <= 256,
  *           T*k <= 512, T*E <= 2048) route and dispatch in one launch;

@@ -43,7 +43,7 @@ class MoeConfig(ctypes.Structure):
                 ("route_path", ctypes.c_int)]
 
 
-GEMM_KERNELS = {"auto": 0, "tc1": 1, "pair": 2, "swap": 3, "ring": 4}
+GEMM_KERNELS = {"auto": 0, "tc1": 1, "pair": 2, "swap": 3}
 ROUTE_PATHS = {"auto": 0, "separate": 1}
 
 
@@ -103,7 +103,7 @@ def _check(rc):
 
 def make_config(cfg: dict) -> MoeConfig:
     """C config from a workload dict (keys T, d, F, E, k, act, dtype, ...;
-    optional gemm_kernel "auto" | "tc1" | "pair" | "swap" | "ring" and route_path
+    optional gemm_kernel "auto" | "tc1" | "pair" | "swap" and route_path
     "auto" | "separate")."""
     return MoeConfig(
         T=int(cfg["T"]), d=int(cfg["d"]), F=int(cfg["F"]), E=int(cfg["E"]), k=int(cfg["k"]),

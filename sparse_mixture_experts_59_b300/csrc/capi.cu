@@ -118,7 +118,7 @@ int check_cfg(const moe_cfg* c) {
         return fail(MOE_ERR_INVALID_ARG, "4-bit expert weights need d and F multiples of 128 (80-byte chunks)%s");
     if (c->weight_fp8 && (c->d % 16 || c->F % 16))
         return fail(MOE_ERR_INVALID_ARG, "FP8 expert weights need d and F multiples of 16 (16-byte rows)%s");
-    if (c->gemm_kernel < MOE_GEMM_AUTO || c->gemm_kernel > MOE_GEMM_RING)
+    if (c->gemm_kernel < MOE_GEMM_AUTO || c->gemm_kernel > MOE_GEMM_SWAP)
         return fail(MOE_ERR_INVALID_ARG, "unknown gemm_kernel%s");
     if (c->route_path != MOE_ROUTE_AUTO && c->route_path != MOE_ROUTE_SEPARATE)
         return fail(MOE_ERR_INVALID_ARG, "unknown route_path%s");
@@ -258,12 +258,11 @@ bool small_front_enabled(const moe_cfg& c) { return c.route_path == MOE_ROUTE_AU
 // over one 256-token tile, which swap would cover with a second tile that
 // re-streams the weights, and decode-sized segments -> tc1.  cfg.gemm_kernel
 // forces one.
-enum GemmKernel { kGemmTc1, kGemmPair, kGemmSwap, kGemmRing };
+enum GemmKernel { kGemmTc1, kGemmPair, kGemmSwap };
 GemmKernel choose_gemm(const moe_cfg& c) {
     if (c.gemm_kernel == MOE_GEMM_TC1) return kGemmTc1;
     if (c.gemm_kernel == MOE_GEMM_PAIR) return kGemmPair;
     if (c.gemm_kernel == MOE_GEMM_SWAP) return kGemmSwap;
-    if (c.gemm_kernel == MOE_GEMM_RING) return kGemmRing;
     const long long rows = (long long)c.T * c.k;
     const long long cap = moe_capacity(&c);
     if (cap >= 0 && cap <= 256 && rows >= 32LL * c.E) return kGemmSwap;   // one tile each
@@ -449,48 +448,6 @@ int run_expert_ffn(const moe_cfg& c, const DevInfo& di, const void* x, const int
     dn.perm_src = perm_src; dn.gate_w = topk_w;
     dn.status = status;
     CUtensorMap maps[6];
-    if (gk == kGemmRing) {
-        // maps: W, W3, W_sh, W3_sh, X (boxes of 128, 64, 32, 16 rows), X_sh (same)
-        CUtensorMap rm[12];
-        auto token_maps = [&](CUtensorMap* out, const void* base, uint64_t rows, int K,
-                              const char* what) {
-            for (int b = 0; b < 4; ++b) {
-                const int rc = encode_rows(&out[b], base, rows, (uint64_t)K, what, 128u >> b);
-                if (rc != MOE_OK) return rc;
-            }
-            return (int)MOE_OK;
-        };
-        const uint32_t wb_up = (uint32_t)ffn_ring_weight_box_rows(up_mode);
-        MOE_TRY(encode_rows(&rm[0], w.W1, (uint64_t)c.E * c.F, c.d, "W1", wb_up));
-        MOE_TRY(encode_rows(&rm[1], c.act == MOE_SWIGLU ? w.W3 : w.W1, (uint64_t)c.E * c.F, c.d,
-                            "W3", wb_up));
-        MOE_TRY(token_maps(&rm[4], Xp, (uint64_t)A, c.d, "gathered rows"));
-        if (rows_sh) {
-            MOE_TRY(encode_rows(&rm[2], w.S1, (uint64_t)c.F_shared, c.d, "S1", wb_up));
-            MOE_TRY(encode_rows(&rm[3], w.S3, (uint64_t)c.F_shared, c.d, "S3", wb_up));
-            MOE_TRY(token_maps(&rm[8], x, (uint64_t)c.T, c.d, "x"));
-        } else {
-            rm[2] = rm[0]; rm[3] = rm[1];
-            for (int b = 0; b < 4; ++b) rm[8 + b] = rm[4 + b];
-        }
-        MOE_CUDA(launch_ffn_ring(up_mode, rm, up, st), "up-projection launch");
-        if (ev) MOE_CUDA(cudaEventRecord(ev[1], st), "event record");
-        const uint32_t wb_dn = (uint32_t)ffn_ring_weight_box_rows(kModeDown);
-        MOE_TRY(encode_rows(&rm[0], w.W2, (uint64_t)c.E * c.d, c.F, "W2", wb_dn));
-        rm[1] = rm[0];
-        MOE_TRY(token_maps(&rm[4], H, (uint64_t)A, c.F, "hidden rows"));
-        if (rows_sh) {
-            MOE_TRY(encode_rows(&rm[2], w.S2, (uint64_t)c.d, c.F_shared, "S2", wb_dn));
-            rm[3] = rm[2];
-            MOE_TRY(token_maps(&rm[8], Hsh, (uint64_t)c.T, c.F_shared, "shared hidden rows"));
-        } else {
-            rm[2] = rm[0]; rm[3] = rm[1];
-            for (int b = 0; b < 4; ++b) rm[8 + b] = rm[4 + b];
-        }
-        MOE_CUDA(launch_ffn_ring(kModeDown, rm, dn, st), "down-projection launch");
-        if (ev) MOE_CUDA(cudaEventRecord(ev[2], st), "event record");
-        return MOE_OK;
-    }
     if (gk == kGemmSwap) {
         // maps: W, W3, X (token rows), W_sh, W3_sh, X_sh
         const uint32_t wb_up = (uint32_t)ffn_swap_weight_box_rows(up_mode);

@@ -170,12 +170,5 @@ cudaError_t launch_ffn_tc2(int mode, const CUtensorMap* maps, const TcFfnArgs& p
 // expert's W_sh, W3_sh, X_sh; weight maps with ffn_swap_weight_box_rows rows
 int ffn_swap_weight_box_rows(int mode);
 cudaError_t launch_ffn_swap(int mode, const CUtensorMap* maps, const TcFfnArgs& p, cudaStream_t st);
-// ffn_ring.cu: weights on M, one token tile of up to 320 rows per segment on
-// N, accumulators from a ring of TMEM columns (many short segments).
-// maps (12): W, W3, W_sh, W3_sh (boxes of ffn_ring_weight_box_rows rows; W3 =
-// W unless SwiGLU), then the token rows X with boxes of 128, 64, 32 and 16
-// rows, then the shared expert's X_sh the same way.
-int ffn_ring_weight_box_rows(int mode);
-cudaError_t launch_ffn_ring(int mode, const CUtensorMap* maps, const TcFfnArgs& p, cudaStream_t st);
 
 }  // namespace moe

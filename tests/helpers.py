@@ -49,8 +49,8 @@ SMALL = {
                                     scoring="sigmoid", renorm=False, capacity_factor=1.0,
                                     seed=2012),
     "decode_switch_bias": dict(base="switch_skewed", T=64, d=128, F=256, E=16, k=1, seed=2013),
-    # segments of ~440 rows (two token tiles each in the 320-row tile kernel)
-    # and a 1100-row shared expert (four tiles of 275 rows: the TMEM ring wraps)
+    # segments of ~440 rows (two 256-row tiles each, the second ragged) and a
+    # 1100-row shared expert over several tiles
     "long_segments_shared": dict(base="fine_grained", T=1100, d=320, F=192, E=5, k=2,
                                  F_shared=192, seed=2014),
 }

@@ -17,10 +17,9 @@ WANT = ("logits", "topk_idx", "topk_w", "counts_pre", "counts_kept", "drop_mask"
 def _params():
     """Each small workload with the library's own GEMM choice, and the bf16
     ones again with each tensor-core GEMM kernel forced (1-SM tokens-on-M,
-    2-SM tokens-on-M, 2-SM weights-on-M, 2-SM weights-on-M with a token tile
-    per segment)."""
+    2-SM tokens-on-M, 2-SM weights-on-M)."""
     out = list(SMALL)
-    for kern in ("tc1", "pair", "swap", "ring"):
+    for kern in ("tc1", "pair", "swap"):
         out += [n + "@" + kern for n in SMALL if small_cfg(n)["dtype"] == "bf16"]
     return out
 
