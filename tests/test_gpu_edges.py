@@ -1,6 +1,11 @@
 """GPU edge cases: tiny and ragged token counts, one expert, k = E, an
-all-ties router, capacity 1, dispatch over many look-back blocks, and bad
-expert indices (reported as a device status; the context stays usable)."""
+all-ties router, capacity 1, dispatch over many look-back blocks, bad expert
+indices (reported as a device status; the context stays usable), bounded
+waits that run out in dispatch and in each expert GEMM kernel (status
+MOE_ERR_DEVICE_TIMEOUT, then a clean call), and guard regions around every
+output buffer."""
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -186,3 +191,72 @@ def test_gemm_wait_times_out_and_reports(kern, low, hold):
     y = layer.forward(inp["x"])["y"]
     assert binding.device_status(layer.ws) == 0
     assert torch.equal(y, ref)
+
+
+GUARD = 4096            # guard bytes before and after each output
+
+
+def _guarded(shape, dtype, fill=0):
+    """A tensor of `shape` inside a larger byte buffer whose GUARD bytes before
+    and after it hold 0xA5, so a write past either end shows.  Returns (view,
+    check) where check() asserts that both guards are intact."""
+    n = int(np.prod(shape)) * torch.tensor([], dtype=dtype).element_size()
+    raw = torch.full((GUARD + n + GUARD,), 0xA5, dtype=torch.uint8, device="cuda")
+    view = raw[GUARD:GUARD + n].view(dtype).view(*shape)
+    view.fill_(fill)
+
+    def check():
+        torch.cuda.synchronize()
+        assert bool((raw[:GUARD] == 0xA5).all()), "guard before the buffer overwritten"
+        assert bool((raw[GUARD + n:] == 0xA5).all()), "guard after the buffer overwritten"
+    return view, check
+
+
+@pytest.mark.parametrize("kern", ["tc1", "pair", "swap"])
+@pytest.mark.parametrize("name,over", [("mixtral_prefill", dict(T=129, d=264, F=392, E=6, k=2)),
+                                       ("fine_grained", dict(T=77, d=192, F=136, E=16, k=4,
+                                                             F_shared=72)),
+                                       ("switch_skewed", dict(T=300, d=128, F=264, E=8, k=1))])
+def test_outputs_stay_inside_their_buffers(name, over, kern):
+    """Canary check: every output of the layer call and of the four stage calls
+    sits between guard regions; ragged shapes (T, d, F and segment lengths off
+    every tile size) must leave the guards untouched."""
+    cfg = workloads.config(name, seed=321, gemm_kernel=kern, **over)
+    inp = workloads.make_inputs(cfg, device="cuda")
+    T, d, E, k = cfg["T"], cfg["d"], cfg["E"], cfg["k"]
+    A = T * k
+    dt = inp["x"].dtype
+    i32, f32, u8 = torch.int32, torch.float32, torch.uint8
+    outs, checks = {}, []
+    for key, shape, t in (("y", (T, d), dt), ("logits", (T, E), f32), ("topk_idx", (T, k), i32),
+                          ("topk_w", (T, k), f32), ("counts_pre", (E,), i32),
+                          ("counts_kept", (E,), i32), ("drop_mask", (A,), u8), ("stats", (2,), f32)):
+        outs[key], chk = _guarded(shape, t)
+        checks.append(chk)
+    layer = binding.MoeLayer(cfg, inp)
+    layer.forward(inp["x"], outputs=outs)
+    assert binding.device_status(layer.ws) == 0
+    for chk in checks:
+        chk()
+    # the stage calls, each output guarded
+    c = binding.make_config(cfg)
+    ws = binding.new_workspace(c)
+    ro = binding.route(c, inp["x"], inp["Wr"], inp.get("logit_bias"), ws=ws)
+    do = binding.dispatch(c, ro["topk_idx"], ro["prob_mean"], ws=ws)
+    Ys, chk_ys = _guarded((A, d), dt)
+    Sh, chk_sh = (_guarded((T, d), dt) if cfg.get("F_shared") else (None, None))
+    w = binding._weights_struct(inp)
+    binding._check(binding.lib().moe_expert_ffn(
+        ctypes.byref(c), binding._p(inp["x"]), binding._p(do["perm_src"]), binding._p(do["offsets"]),
+        binding._p(ro["topk_w"]), ctypes.byref(w), binding._p(Ys), binding._p(Sh), binding._p(ws),
+        ws.numel(), binding._stream()))
+    y2, chk_y2 = _guarded((T, d), dt)
+    binding._check(binding.lib().moe_combine(
+        ctypes.byref(c), binding._p(inp["x"]), binding._p(Ys), binding._p(do["drop_mask"]),
+        binding._p(Sh), binding._p(y2), binding._stream()))
+    assert binding.device_status(ws) == 0
+    chk_ys()
+    chk_y2()
+    if chk_sh:
+        chk_sh()
+    assert torch.equal(y2, outs["y"])
