@@ -365,8 +365,7 @@ int run_expert_ffn(const moe_cfg& c, const DevInfo& di, const void* x, const int
                  "gather launch");
         if (ev) MOE_CUDA(cudaEventRecord(ev[0], st), "event record");
         CUtensorMap maps[3];
-        const uint32_t tbox = (uint32_t)ffn_fp8_token_box_rows();
-        MOE_TRY(encode_rows(&maps[0], Xp, (uint64_t)A, c.d, "gathered rows", tbox,
+        MOE_TRY(encode_rows(&maps[0], Xp, (uint64_t)A, c.d, "gathered rows", 16,
                             CU_TENSOR_MAP_DATA_TYPE_FLOAT16));
         MOE_TRY(wmap(&maps[1], w.W1, (uint64_t)c.E * c.F, c.d, "W1"));
         MOE_TRY(wmap(&maps[2], c.act == MOE_SWIGLU ? w.W3 : w.W1, (uint64_t)c.E * c.F, c.d, "W3"));
@@ -385,7 +384,7 @@ int run_expert_ffn(const moe_cfg& c, const DevInfo& di, const void* x, const int
         up.hold = at<int>(ws, L.ctrl) + kCtrlHoldGemm;
         MOE_CUDA(launch_ffn_fp8(up_mode, maps, up, di.num_sms, st, fp4), "up-projection launch");
         if (ev) MOE_CUDA(cudaEventRecord(ev[1], st), "event record");
-        MOE_TRY(encode_rows(&maps[0], H, (uint64_t)A, c.F, "hidden rows", tbox,
+        MOE_TRY(encode_rows(&maps[0], H, (uint64_t)A, c.F, "hidden rows", 16,
                             CU_TENSOR_MAP_DATA_TYPE_FLOAT16));
         MOE_TRY(wmap(&maps[1], w.W2, (uint64_t)c.E * c.d, c.F, "W2"));
         maps[2] = maps[1];

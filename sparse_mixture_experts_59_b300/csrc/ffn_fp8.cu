@@ -93,7 +93,7 @@ constexpr int WROWS = 128;                     // weight rows per block (MMA M, 
 constexpr int G = 4;                           // weight blocks per tile
 constexpr int NISS = 2;                        // MMA issuers, blocks i, i + NISS, ...
 constexpr int TOK = 32;                        // tokens per tile at most (MMA N)
-constexpr int TOK_BOX = 8;                     // token rows per TMA box (a CTA's half of 16)
+constexpr int TOK_BOX = 16;                    // token rows per TMA box
 constexpr int TB_BYTES = 24 * 1024;            // token chunk buffer (two of them)
 constexpr int A_COLS = BK / 2;                 // TMEM columns of one A buffer (f16 pairs)
 constexpr int ACC_SET = G * TOK;               // TMEM columns of a tile's accumulators
@@ -101,8 +101,6 @@ constexpr int A_COL0 = 2 * ACC_SET;            // two accumulator sets, then the
 constexpr int TMEM_COLS = 512;
 static_assert(A_COL0 + G * A_COLS <= TMEM_COLS, "tensor memory budget (an A buffer per block)");
 constexpr int TOKP_WARP = 1;                   // token producer (and TMEM owner)
-constexpr uint16_t BOTH = 0x3;                 // both CTAs of the pair
-constexpr uint16_t LEADER_ONLY = 0x1;
 constexpr int XCH_LD = 33;
 
 // Weight formats.  Both give a stage 128 values of each weight row (one MMA K
@@ -173,17 +171,15 @@ struct Seg {
     int g;             // expert
     int tok0, ntok;    // first gathered row, valid tokens
     int nmma;          // MMA N: ntok rounded up to 16
-    int blk0, nblk;    // first pair block (within the expert), pair blocks in the tile
+    int blk0, nblk;    // first weight block (within the expert), blocks in the tile
     int kb0, kb1;
-    int c_first, c_last;  // pairs whose ranges meet the tile
+    int c_first, c_last;  // CTAs whose ranges meet the tile
 };
 
-// Tiles enumerate (expert, group of G pair blocks, token tile), token tile
-// fastest.  A pair block is 256 weight rows: 128 in each CTA of the pair
-// (nwbp pair blocks per expert); W work units are split over ncl pairs.
+// Tiles enumerate (expert, block group, token tile), token tile fastest.
 __device__ __forceinline__ Seg decode_seg(const TcFfnArgs& p, const int* s_start, const int* s_off,
-                                          int nwbp, int nk, long long W, int ncl, int tile,
-                                          int kb0, int kb1) {
+                                          int nwb, int nk, long long W, int tile, int kb0,
+                                          int kb1) {
     Seg t;
     t.tile = tile;
     t.g = find_group(s_start, p.E, tile);
@@ -196,24 +192,19 @@ __device__ __forceinline__ Seg decode_seg(const TcFfnArgs& p, const int* s_start
     t.ntok = min(TOK, rows - tt * TOK);
     t.nmma = (t.ntok + 15) & ~15;
     t.blk0 = wbg * G;
-    t.nblk = min(G, nwbp - t.blk0);
+    t.nblk = min(G, nwb - t.blk0);
     t.kb0 = kb0;
     t.kb1 = kb1;
-    t.c_first = cta_of((long long)tile * nk, W, ncl);
-    t.c_last = cta_of((long long)tile * nk + nk - 1, W, ncl);
+    const int grid = (int)gridDim.x;
+    t.c_first = cta_of((long long)tile * nk, W, grid);
+    t.c_last = cta_of((long long)tile * nk + nk - 1, W, grid);
     return t;
 }
 
-// This CTA's 128-row block of pair block j of a tile (rank 0 the first half).
-__device__ __forceinline__ int cta_block(const Seg& t, int j, int rank) {
-    return 2 * (t.blk0 + j) + rank;
-}
-
-// Weight rows of this CTA's block of pair block j: the first rows of its two
-// 64-row boxes.
+// Weight rows of block j of a tile: the first rows of its two 64-row boxes.
 template <int MODE>
-__device__ __forceinline__ int2 block_rows(const TcFfnArgs& p, const Seg& t, int j, int rank) {
-    const int u0 = cta_block(t, j, rank) * Fp8Traits<MODE>::UNITS;
+__device__ __forceinline__ int2 block_rows(const TcFfnArgs& p, const Seg& t, int j) {
+    const int u0 = (t.blk0 + j) * Fp8Traits<MODE>::UNITS;
     const int r0 = t.g * p.N + u0;
     return make_int2(r0, MODE == kModeSwiglu ? r0 : r0 + 64);
 }
@@ -226,10 +217,10 @@ __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: 
 // row, into its own slots of the prefetch area.
 template <int MODE>
 __device__ __forceinline__ void prefetch_rows(const TcFfnArgs& p, const Seg& t, int row,
-                                              float* s_pre, int rank) {
+                                              float* s_pre) {
     const size_t sbase = (size_t)t.g * p.N;
     for (int j = 0; j < t.nblk; ++j) {
-        const int u0 = cta_block(t, j, rank) * Fp8Traits<MODE>::UNITS;
+        const int u0 = (t.blk0 + j) * Fp8Traits<MODE>::UNITS;
         float sc = 0.f, b = 0.f;
         if (MODE == kModeSwiglu) {
             const int u = u0 + (row & 63);
@@ -249,8 +240,8 @@ __device__ __forceinline__ void prefetch_rows(const TcFfnArgs& p, const Seg& t, 
 template <int MODE>
 __device__ __forceinline__ void finish_block(const TcFfnArgs& p, const Seg& t, int j, int row,
                                              float (&v)[32], float* s_xch, const float* s_pre,
-                                             const int* s_tok_a, const float* s_tok_w, int rank) {
-    const int u0 = cta_block(t, j, rank) * Fp8Traits<MODE>::UNITS;
+                                             const int* s_tok_a, const float* s_tok_w) {
+    const int u0 = (t.blk0 + j) * Fp8Traits<MODE>::UNITS;
     const float sc = s_pre[j * WROWS + row];
     if (MODE == kModeSwiglu) {
         const int u = u0 + (row & 63);
@@ -324,25 +315,22 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
     int* s_off = reinterpret_cast<int*>(smem + F::OFF_OFFS);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int rank = (int)ptx::cluster_ctarank();
-    const bool leader = (rank == 0);
-    const int cluster = (int)blockIdx.x >> 1, ncl = (int)gridDim.x >> 1;
     if (threadIdx.x == 0) {
         for (int s = 0; s < F::WSTAGES; ++s) {
             ptx::mbar_init(&wfull[s], 1);
             ptx::mbar_init(&wempty[s], F::CVT_WARPS);
         }
         for (int s = 0; s < 2; ++s) {
-            ptx::mbar_init(&kfull[s], 1);         // the leader's: both CTAs' token bytes
-            ptx::mbar_init(&kempty[s], NISS);     // one commit per issuer (to both CTAs)
+            ptx::mbar_init(&kfull[s], 1);
+            ptx::mbar_init(&kempty[s], NISS);
         }
         for (int b = 0; b < G; ++b) {
-            ptx::mbar_init(&cfull[b], 2 * F::CVT_WARPS);   // the leader's: both CTAs' converters
+            ptx::mbar_init(&cfull[b], F::CVT_WARPS);
             ptx::mbar_init(&cempty[b], 1);
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(&tfull[a], NISS);
-            ptx::mbar_init(&tempty[a], 2 * 128);   // the leader's: both CTAs' epilogue threads
+            ptx::mbar_init(&tempty[a], 128);
         }
         for (int j = 0; j < NISS; ++j) ptx::mbar_init(&drain[j], 1);
         *s_abort = 0;
@@ -352,8 +340,8 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
         ptx::prefetch_tensormap(&mapW3);
     }
     if (warp == 1) {
-        ptx::tmem_alloc_pair(s_tmem, TMEM_COLS);
-        ptx::tmem_relinquish_pair();
+        ptx::tmem_alloc(s_tmem, TMEM_COLS);
+        ptx::tmem_relinquish();
     }
     // Only the token rows come from the kernel just before this one (the
     // gather, or the up projection for the down projection): the offsets,
@@ -366,7 +354,6 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
     for (int i = threadIdx.x; i <= p.E; i += F::NUM_THREADS) s_off[i] = p.offsets[i];
     __syncthreads();
     const int nwb = (p.N + Fp8Traits<MODE>::UNITS - 1) / Fp8Traits<MODE>::UNITS;
-    const int nwbp = (nwb + 1) / 2;                 // pair blocks per expert
     if (warp == 0) {            // longest segment: sizes the token chunks
         int m = 0;
         for (int g = lane; g < p.E; g += 32) m = max(m, s_off[g + 1] - s_off[g]);
@@ -374,27 +361,22 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
         for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
         if (lane == 0) *s_maxrows = m;
     }
-    group_tile_prefix(s_off, p.E, 0, TOK, (nwbp + G - 1) / G, 0, s_start);
-    // both CTAs' barriers initialised and TMEM allocated before any
-    // cross-CTA arrive, copy or MMA
+    group_tile_prefix(s_off, p.E, 0, TOK, (nwb + G - 1) / G, 0, s_start);
     ptx::tc_fence_before();
-    __syncwarp();
-    ptx::cluster_sync();
+    __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *s_tmem;
+    const int grid = (int)gridDim.x;
     const int nk = (p.K + BK - 1) / BK;
     const long long W = (long long)s_start[p.E] * nk;
-    const long long my0 = cta_start(W, ncl, cluster);
-    const long long my1 = cta_start(W, ncl, cluster + 1);
-    const uint32_t kfull_leader = ptx::mapa_shared(ptx::smem_u32(kfull), 0);
-    const uint32_t cfull_leader = ptx::mapa_shared(ptx::smem_u32(cfull), 0);
-    const uint32_t tempty_leader = ptx::mapa_shared(ptx::smem_u32(tempty), 0);
+    const long long my0 = cta_start(W, grid, blockIdx.x);
+    const long long my1 = cta_start(W, grid, blockIdx.x + 1);
     const long long slot_floats = (long long)WROWS * TOK;              // one block's partials
-    // k-blocks per token chunk: a CTA's half of the widest token tile fills a buffer
-    const int CH = TB_BYTES / (min(TOK, max(16, (*s_maxrows + 15) & ~15)) / 2 * 256);
-    // room for two slots of G blocks per CTA and a ticket per (pair, rank)
-    const bool room = p.split_ticket && (int)gridDim.x <= p.split_tickets &&
-                      2LL * (int)gridDim.x * G * slot_floats * 4 <= p.split_bytes;
+    // k-blocks per token chunk: the widest token tile fills a buffer
+    const int CH = TB_BYTES / (min(TOK, max(16, (*s_maxrows + 15) & ~15)) * 256);
+    // room for two slots of G blocks per CTA and a ticket per CTA
+    const bool room = p.split_ticket && grid <= p.split_tickets &&
+                      2LL * grid * G * slot_floats * 4 <= p.split_bytes;
     long long end = my1;
     if (!room && W > 0) {
         if (threadIdx.x == 0) raise_error(p.status, MOE_ERR_INVALID_ARG);
@@ -429,7 +411,7 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
     for (int si_ = 0; si_ < nseg; ++si_) {                                                 \
         int tile_, kb0_, kb1_;                                                             \
         seg_of(si_, tile_, kb0_, kb1_);                                                    \
-        const Seg t = decode_seg(p, s_start, s_off, nwbp, nk, W, ncl, tile_, kb0_, kb1_);
+        const Seg t = decode_seg(p, s_start, s_off, nwb, nk, W, tile_, kb0_, kb1_);
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer (weights)
@@ -445,7 +427,7 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
                         const uint32_t ph = (uint32_t)(it / F::WSTAGES) & 1u;
                         if (!ptx::mbar_wait_nap(&wempty[s], ph ^ 1u, s_abort, 64)) { ok = false; break; }
                         ptx::mbar_arrive_expect_tx(&wfull[s], F::WQ_BYTES);
-                        const int2 wr = block_rows<MODE>(p, t, j, rank);
+                        const int2 wr = block_rows<MODE>(p, t, j);
                         uint8_t* wq = sWq + s * F::WQ_BYTES;
                         ptx::tma_load_2d(wq, &mapW, &wfull[s], kb * F::ROW_BYTES, wr.x);
                         ptx::tma_load_2d(wq + F::WQ_BYTES / 2, &mapW3, &wfull[s], kb * F::ROW_BYTES, wr.y);
@@ -469,8 +451,7 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
             int cc = 0;
             bool ok = true;
             FOR_EACH_SEG(t)
-                const int half = t.nmma / 2;         // this CTA's token rows of the tile
-                const int atom = half * 128;
+                const int atom = t.nmma * 128;
                 for (int kc = t.kb0; kc < t.kb1; kc += CH, ++cc) {
                     const int kend = min(kc + CH, t.kb1);
                     const int ub = cc & 1;
@@ -478,16 +459,13 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
                         ok = false;
                         break;
                     }
-                    // both CTAs' halves land on the leader's barrier
-                    if (leader)
-                        ptx::mbar_arrive_expect_tx(&kfull[ub], (uint32_t)((kend - kc) * 2 * atom * 2));
+                    ptx::mbar_arrive_expect_tx(&kfull[ub], (uint32_t)((kend - kc) * 2 * atom));
                     uint8_t* tb = sTok + ub * TB_BYTES;
-                    const uint32_t fb = kfull_leader + 8u * (uint32_t)ub;
                     for (int kb = kc; kb < kend; ++kb)
                         for (int a = 0; a < 2; ++a)
-                            for (int r = 0; r < half; r += TOK_BOX)
-                                ptx::tma_load_2d_pair(tb + (2 * (kb - kc) + a) * atom + r * 128, &mapX,
-                                                      fb, kb * BK + a * 64, t.tok0 + rank * half + r);
+                            for (int r = 0; r < t.nmma; r += TOK_BOX)
+                                ptx::tma_load_2d(tb + (2 * (kb - kc) + a) * atom + r * 128, &mapX,
+                                                 &kfull[ub], kb * BK + a * 64, t.tok0 + r);
                 }
                 if (!ok) break;
             }
@@ -495,9 +473,8 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
                 *s_abort = 1;
                 raise_error(p.status, MOE_ERR_DEVICE_TIMEOUT);
             }
-            if (leader)
-                for (int j = (cc > 2 ? cc - 2 : 0); j < cc; ++j)
-                    ptx::mbar_wait(&kfull[j & 1], (uint32_t)(j >> 1) & 1u, nullptr);
+            for (int j = (cc > 2 ? cc - 2 : 0); j < cc; ++j)
+                ptx::mbar_wait(&kfull[j & 1], (uint32_t)(j >> 1) & 1u, nullptr);
         }
     } else if (warp >= F::MMA_WARP0) {
         // ------------------------------------------------------- MMA issuers
@@ -506,7 +483,7 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
         // still arrives on the tile's shared barriers (token chunks,
         // accumulators).
         const int mi = warp - F::MMA_WARP0;
-        if (leader && lane == 0) {
+        if (lane == 0) {
             uint32_t nfill = 0;                 // bit j: parity of block j's fills so far
             int tc = 0, cc = 0;                 // tiles, token chunks
             bool ok = true;
@@ -514,10 +491,11 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
                 const int acc = tc & 1;
                 const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
                 ++tc;
+                const bool mine = mi < t.nblk;
                 if (!ptx::mbar_wait_nap(&tempty[acc], aph ^ 1u, s_abort, 64)) { ok = false; break; }
                 ptx::tc_fence_after();
-                const uint32_t idesc = ptx::idesc_f16_f32(2 * WROWS, t.nmma);   // M = 256 on the pair
-                const int atom = (t.nmma / 2) * 128;
+                const uint32_t idesc = ptx::idesc_f16_f32(WROWS, t.nmma);
+                const int atom = t.nmma * 128;
                 const uint8_t* tb = sTok;
                 int kc = t.kb0;
                 for (int kb = t.kb0; ok && kb < t.kb1; ++kb) {
@@ -543,29 +521,31 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
                         const uint32_t d_tmem =
                             tmem_base + (uint32_t)(acc * ACC_SET + j * TOK);
                         const uint32_t a_tmem = tmem_base + (uint32_t)(A_COL0 + j * A_COLS);
-                        ptx::mma_f16_tmem_a_pair(d_tmem, a_tmem + 0, bd0 + 0, idesc, first);
-                        ptx::mma_f16_tmem_a_pair(d_tmem, a_tmem + 8, bd0 + 2, idesc, 1u);
-                        ptx::mma_f16_tmem_a_pair(d_tmem, a_tmem + 16, bd0 + 4, idesc, 1u);
-                        ptx::mma_f16_tmem_a_pair(d_tmem, a_tmem + 24, bd0 + 6, idesc, 1u);
-                        ptx::mma_f16_tmem_a_pair(d_tmem, a_tmem + 32, bd1 + 0, idesc, 1u);
-                        ptx::mma_f16_tmem_a_pair(d_tmem, a_tmem + 40, bd1 + 2, idesc, 1u);
-                        ptx::mma_f16_tmem_a_pair(d_tmem, a_tmem + 48, bd1 + 4, idesc, 1u);
-                        ptx::mma_f16_tmem_a_pair(d_tmem, a_tmem + 56, bd1 + 6, idesc, 1u);
-                        ptx::mma_commit_pair_mc(&cempty[j], BOTH);
+                        ptx::mma_f16_tmem_a(d_tmem, a_tmem + 0, bd0 + 0, idesc, first);
+                        ptx::mma_f16_tmem_a(d_tmem, a_tmem + 8, bd0 + 2, idesc, 1u);
+                        ptx::mma_f16_tmem_a(d_tmem, a_tmem + 16, bd0 + 4, idesc, 1u);
+                        ptx::mma_f16_tmem_a(d_tmem, a_tmem + 24, bd0 + 6, idesc, 1u);
+                        ptx::mma_f16_tmem_a(d_tmem, a_tmem + 32, bd1 + 0, idesc, 1u);
+                        ptx::mma_f16_tmem_a(d_tmem, a_tmem + 40, bd1 + 2, idesc, 1u);
+                        ptx::mma_f16_tmem_a(d_tmem, a_tmem + 48, bd1 + 4, idesc, 1u);
+                        ptx::mma_f16_tmem_a(d_tmem, a_tmem + 56, bd1 + 6, idesc, 1u);
+                        ptx::mma_commit(&cempty[j]);
                     }
                     if (ok && (kb + 1 == t.kb1 || (kb + 1 - t.kb0) % CH == 0)) {   // chunk done
-                        ptx::mma_commit_pair_mc(&kempty[cc & 1], BOTH);   // no MMAs: arrives at once
+                        if (mine) ptx::mma_commit(&kempty[cc & 1]);
+                        else ptx::mbar_arrive(&kempty[cc & 1]);
                         ++cc;
                     }
                 }
                 if (!ok) break;
-                ptx::mma_commit_pair_mc(&tfull[acc], BOTH);
+                if (mine) ptx::mma_commit(&tfull[acc]);
+                else ptx::mbar_arrive(&tfull[acc]);
             }
             if (!ok) {
                 *s_abort = 1;
                 raise_error(p.status, MOE_ERR_DEVICE_TIMEOUT);
             }
-            ptx::mma_commit_pair_mc(&drain[mi], LEADER_ONLY);
+            ptx::mma_commit(&drain[mi]);
             ptx::mbar_wait(&drain[mi], 0, nullptr);
         }
     } else if (warp >= 6) {
@@ -663,7 +643,7 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
                     ptx::tmem_wait_st();                  // the stage's stores, then signal
                     ptx::tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive_cluster(cfull_leader + 8u * (uint32_t)b);
+                    if (lane == 0) ptx::mbar_arrive(&cfull[b]);
                 }
             if (!ok) break;
         }
@@ -683,7 +663,7 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
             ++tc;
             // inputs of the epilogue, while the tile's MMAs run: own row slots,
             // and the token slots into the buffer of this tile's parity
-            prefetch_rows<MODE>(p, t, row, s_pre, rank);
+            prefetch_rows<MODE>(p, t, row, s_pre);
             int* tok_a = s_tok_a + acc * TOK;
             float* tok_w = s_tok_w + acc * TOK;
             if (MODE == kModeDown) {
@@ -713,16 +693,16 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
                     __syncwarp();
                     float v[32];
                     ptx::tmem_ld32(tq + (uint32_t)(j * TOK), v);
-                    finish_block<MODE>(p, t, j, row, v, s_xch, s_pre, tok_a, tok_w, rank);
+                    finish_block<MODE>(p, t, j, row, v, s_xch, s_pre, tok_a, tok_w);
                 }
                 ptx::tc_fence_before();
-                ptx::mbar_arrive_cluster(tempty_leader + 8u * (uint32_t)acc);
+                ptx::mbar_arrive(&tempty[acc]);
                 continue;
             }
             // part of a shared tile: partial sums -> this CTA's slot
             // (0 = the tile of its first segment, 1 = of its last), [block][column][row]
             const int slot = (t.tile == t_first) ? 0 : 1;
-            float* mine = p.split_part + ((size_t)blockIdx.x * 2 + slot) * G * slot_floats;   // own rows
+            float* mine = p.split_part + ((size_t)blockIdx.x * 2 + slot) * G * slot_floats;
             for (int j = 0; j < t.nblk; ++j) {
                 __syncwarp();
                 float v[32];
@@ -732,17 +712,16 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
                     if (c < t.ntok) mine[j * slot_floats + (size_t)c * WROWS + row] = v[c];
             }
             ptx::tc_fence_before();
-            ptx::mbar_arrive_cluster(tempty_leader + 8u * (uint32_t)acc);
+            ptx::mbar_arrive(&tempty[acc]);
             __threadfence();
             epi_bar();
             if (et == 0) {
-                int parts = 0;                               // pairs with work in the tile
+                int parts = 0;                               // CTAs with work in the tile
                 for (int c = t.c_first; c <= t.c_last; ++c)
-                    parts += cta_start(W, ncl, c) < cta_start(W, ncl, c + 1);
-                int* ticket = p.split_ticket + 2 * t.c_last + rank;   // one per (pair, rank)
-                const int prev = atomicAdd(ticket, 1);
+                    parts += cta_start(W, grid, c) < cta_start(W, grid, c + 1);
+                const int prev = atomicAdd(p.split_ticket + t.c_last, 1);
                 const int last = prev == parts - 1;
-                if (last) *ticket = 0;                       // ready for the next launch
+                if (last) p.split_ticket[t.c_last] = 0;      // ready for the next launch
                 *s_last = last;
             }
             epi_bar();
@@ -752,33 +731,28 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
                 float v[32];
 #pragma unroll
                 for (int c = 0; c < 32; ++c) v[c] = 0.f;
-                for (int c = t.c_first; c <= t.c_last; ++c) {   // the same rank of each pair
-                    const long long s0 = cta_start(W, ncl, c);
-                    if (s0 == cta_start(W, ncl, c + 1)) continue;          // no work there
+                for (int cta = t.c_first; cta <= t.c_last; ++cta) {
+                    const long long s0 = cta_start(W, grid, cta);
+                    if (s0 == cta_start(W, grid, cta + 1)) continue;        // no work there
                     const int sl = (t.tile == (int)(s0 / nk)) ? 0 : 1;
-                    const int cta = 2 * c + rank;
                     const float* src =
                         p.split_part + ((size_t)cta * 2 + sl) * G * slot_floats + j * slot_floats;
 #pragma unroll
                     for (int c = 0; c < 32; ++c)
                         if (c < t.ntok) v[c] += __ldcg(src + (size_t)c * WROWS + row);
                 }
-                finish_block<MODE>(p, t, j, row, v, s_xch, s_pre, tok_a, tok_w, rank);
+                finish_block<MODE>(p, t, j, row, v, s_xch, s_pre, tok_a, tok_w);
             }
         }
     }
 #undef FOR_EACH_SEG
 
-    // teardown: both CTAs done (no remote arrive or MMA still targets either),
-    // then each frees its half of the pair's TMEM
     ptx::tc_fence_before();
     __syncthreads();
-    __syncwarp();
-    ptx::cluster_sync();
     if (warp == 1) {
         __syncwarp();
         ptx::tc_fence_after();
-        ptx::tmem_dealloc_pair(tmem_base, TMEM_COLS);
+        ptx::tmem_dealloc(tmem_base, TMEM_COLS);
     }
 }
 
@@ -790,9 +764,9 @@ cudaError_t launch_one(const CUtensorMap* maps, const TcFfnArgs& p, int num_sms,
     const cudaError_t err = cudaFuncSetAttribute(
         kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, WF<FMT>::SMEM_BYTES);
     if (err != cudaSuccess) return err;
-    const int grid = (num_sms < kFp8MaxGrid ? num_sms : kFp8MaxGrid) & ~1;   // CTA pairs
+    const int grid = num_sms < kFp8MaxGrid ? num_sms : kFp8MaxGrid;
     return launch_kernel(kernel, dim3(grid), dim3(WF<FMT>::NUM_THREADS), WF<FMT>::SMEM_BYTES, st,
-                         2, maps[0], maps[1], maps[2], p);
+                         1, maps[0], maps[1], maps[2], p);
 }
 
 template <int FMT>
@@ -802,8 +776,6 @@ cudaError_t launch_fmt(int mode, const CUtensorMap* maps, const TcFfnArgs& p, in
     if (mode == kModeGelu) return launch_one<kModeGelu, FMT>(maps, p, num_sms, st);
     return launch_one<kModeDown, FMT>(maps, p, num_sms, st);
 }
-
-int ffn_fp8_token_box_rows() { return TOK_BOX; }
 
 cudaError_t launch_ffn_fp8(int mode, const CUtensorMap* maps, const TcFfnArgs& p, int num_sms,
                            cudaStream_t st, bool fp4) {

@@ -153,9 +153,8 @@ cudaError_t launch_ffn_tc(int mode, const CUtensorMap* maps, const TcFfnArgs& p,
 // ffn_fp8.cu: FP8 (E4M3) weights with per-row scales, weights on the MMA's M;
 // at most kFp8MaxGrid CTAs (its partial-sum slots: 2 per CTA of 4 weight blocks
 // x 128 rows x 32 tokens fp32, and one ticket per CTA)
-// maps: X (f16 token rows, box 64 x ffn_fp8_token_box_rows()), W and W3 (E4M3
-// rows, box 128 bytes x 64 rows; W3 = W for GELU / down), all with the 128-byte
-// swizzle.  Runs on CTA pairs (cluster of 2, cta_group::2 MMAs, M = 256).
+// maps: X (f16 token rows, box 64 x 16), W and W3 (E4M3 rows, box 128 bytes x
+// 64 rows; W3 = W for GELU / down), all with the 128-byte swizzle
 constexpr int kFp8MaxGrid = 160;
 constexpr size_t kFp8SplitBytes = (size_t)2 * kFp8MaxGrid * 4 * 128 * 32 * 4;
 // fp4: packed E2M1 weights (rows of 80-byte chunks: 64 code bytes, 8 E4M3 block
@@ -163,9 +162,6 @@ constexpr size_t kFp8SplitBytes = (size_t)2 * kFp8MaxGrid * 4 * 128 * 32 * 4;
 // no swizzle) instead of E4M3
 cudaError_t launch_ffn_fp8(int mode, const CUtensorMap* maps, const TcFfnArgs& p, int num_sms,
                            cudaStream_t st, bool fp4 = false);
-// token rows per box of the low-bit kernels' token map (a CTA's half of the
-// smallest token tile)
-int ffn_fp8_token_box_rows();
 // ffn_tc2.cu: the same on CTA pairs (cta_group::2), 256-row tiles; same maps
 int ffn_tc2_tile_rows();
 cudaError_t launch_ffn_tc2(int mode, const CUtensorMap* maps, const TcFfnArgs& p, cudaStream_t st);

@@ -79,21 +79,6 @@ __device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem,
         : "memory");
 }
 
-// The same on a CTA pair (cta_group::2, M = 256): each CTA's TMEM holds the A
-// rows and accumulator rows of its own 128 lanes at the same addresses, and B
-// is split between the two CTAs' shared memory (N / 2 rows each).  Issued by
-// one thread of the even CTA.
-__device__ __forceinline__ void mma_f16_tmem_a_pair(uint32_t d_tmem, uint32_t a_tmem,
-                                                    uint64_t b_desc, uint32_t idesc,
-                                                    uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
 // 16 consecutive 32-bit columns of the warp's 32 lanes <- v (one lane per
 // thread), then waits until the stores are done.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
