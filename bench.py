@@ -819,7 +819,8 @@ def run_sweep(args, world, local):
             outputs = {"y": torch.empty_like(inp["x"]),
                        "counts_kept": torch.empty(cfg["E"], dtype=torch.int32, device=dev)}
             steps = max(10, min(args.steps, 50))
-            ms, stages, _ = time_layer(layer, inp["x"], steps, args.warmup, world, outputs)
+            ms, stages, _ = time_layer(layer, inp["x"], steps, args.warmup, world, outputs,
+                                       settle_s=0.25)
             R = int(outputs["counts_kept"].sum().item())
             hit = int((outputs["counts_kept"] > 0).sum().item())
             alg = algorithmic(cfg, R)
