@@ -252,11 +252,13 @@ bool small_front_enabled(const moe_cfg& c) { return c.route_path == MOE_ROUTE_AU
 //   kGemmPair  2-SM kernel, tokens on M in 256-row tiles (ffn_tc2.cu)
 //   kGemmSwap  2-SM kernel, weights on M and tokens on N (ffn_swap.cu): a
 //              segment's last tile shrinks to a multiple of 32 tokens
-// Automatic choice (from B300 measurements of the five workloads): segments
-// of at most 256 rows on average that fit one token tile (capacity-limited
-// layers) -> swap; long segments (>= 512 rows) -> swap; segments a little
-// over one 256-token tile, which swap would cover with a second tile that
-// re-streams the weights, and decode-sized segments -> tc1.  cfg.gemm_kernel
+// Automatic choice (from B300 measurements: the five workloads and a sweep of
+// the token count on Mixtral-shaped weights): capacity-limited segments that
+// fit one token tile -> swap; long segments (>= 512 rows on average) -> swap;
+// at most one row per expert (a few tokens) -> swap; 128+ rows per expert on
+// few (<= 16) experts -> swap; otherwise tc1 (decode-sized segments of a few
+// rows, and many experts with ~256-row segments, where swap's second, ragged
+// token tile costs more than tc1's ragged 128-row tile).  cfg.gemm_kernel
 // forces one.
 enum GemmKernel { kGemmTc1, kGemmPair, kGemmSwap };
 GemmKernel choose_gemm(const moe_cfg& c) {
@@ -267,6 +269,8 @@ GemmKernel choose_gemm(const moe_cfg& c) {
     const long long cap = moe_capacity(&c);
     if (cap >= 0 && cap <= 256 && rows >= 32LL * c.E) return kGemmSwap;   // one tile each
     if (rows >= 512LL * c.E) return kGemmSwap;
+    if (rows <= c.E) return kGemmSwap;
+    if (c.E <= 16 && rows >= 128LL * c.E) return kGemmSwap;
     return kGemmTc1;
 }
 
