@@ -150,23 +150,59 @@ router_topk_kernel(const float* part, int nsplit, const float* __restrict__ bias
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    // column sums of prob_part[nblocks][E]: thread t adds rows g, g+G, ...
-    // (g = t / E, G = 256 / E groups) for expert t % E, then the groups are
-    // added in order -- a fixed order, so the result repeats exactly
-    const int G = blockDim.x / E > 0 ? (int)blockDim.x / E : 1;
+    // column sums of prob_part[nblocks][E], in a fixed order so that the
+    // result repeats exactly.  One block reads all nblocks x E partials (up to
+    // 1024 x 256), so the loads go 16 bytes and 8 at a time: with E a multiple
+    // of 4, thread t adds rows g, g+G, ... (g = t / C, G = 256 / C groups) of
+    // the 4 experts of float4 column t % C (C = E / 4), then the groups are
+    // added in order; otherwise one expert per thread the same way.
     float* s_col = &s_psum[0][0];                  // reuse: [G][E] partial columns
-    if ((int)threadIdx.x < G * E) {
-        const int e = threadIdx.x % E, g = threadIdx.x / E;
-        float a8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // 8 loads in flight
-        int b = g;
-        for (; b + 7 * G < (int)gridDim.x; b += 8 * G)
+    const int nb = (int)gridDim.x;
+    int G;
+    if ((E & 3) == 0) {
+        const int C = E / 4;
+        G = (int)blockDim.x / C > 0 ? (int)blockDim.x / C : 1;
+        if ((int)threadIdx.x < G * C) {
+            const int c = threadIdx.x % C, g = threadIdx.x / C;
+            const float4* src = reinterpret_cast<const float4*>(prob_part) + c;
+            float4 a[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) a8[j] += __ldcg(prob_part + (size_t)(b + j * G) * E + e);
-        for (; b < (int)gridDim.x; b += G) a8[0] += __ldcg(prob_part + (size_t)b * E + e);
-        float acc = 0.f;
+            for (int j = 0; j < 8; ++j) a[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            int b = g;
+            for (; b + 7 * G < nb; b += 8 * G) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc += a8[j];
-        s_col[g * E + e] = acc;
+                for (int j = 0; j < 8; ++j) {
+                    const float4 v = __ldcg(src + (size_t)(b + j * G) * C);
+                    a[j].x += v.x; a[j].y += v.y; a[j].z += v.z; a[j].w += v.w;
+                }
+            }
+            for (; b < nb; b += G) {
+                const float4 v = __ldcg(src + (size_t)b * C);
+                a[0].x += v.x; a[0].y += v.y; a[0].z += v.z; a[0].w += v.w;
+            }
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                acc.x += a[j].x; acc.y += a[j].y; acc.z += a[j].z; acc.w += a[j].w;
+            }
+            float* dst = s_col + g * E + 4 * c;
+            dst[0] = acc.x; dst[1] = acc.y; dst[2] = acc.z; dst[3] = acc.w;
+        }
+    } else {
+        G = (int)blockDim.x / E > 0 ? (int)blockDim.x / E : 1;
+        if ((int)threadIdx.x < G * E) {
+            const int e = threadIdx.x % E, g = threadIdx.x / E;
+            float a8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // 8 loads in flight
+            int b = g;
+            for (; b + 7 * G < nb; b += 8 * G)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) a8[j] += __ldcg(prob_part + (size_t)(b + j * G) * E + e);
+            for (; b < nb; b += G) a8[0] += __ldcg(prob_part + (size_t)b * E + e);
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc += a8[j];
+            s_col[g * E + e] = acc;
+        }
     }
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
