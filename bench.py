@@ -424,7 +424,7 @@ def run_ours(args, world, rank, local):
     kname = "up_gemm/%s" % (args.gemm or "auto")
     traffic, digest = recorded_traffic(args.workload, kname) if args.tokens is None and \
         args.experts is None else (None, None)
-    mhz = clk["sm_mhz"] if clk else None
+    mhz = clk.get("sm_mhz") if clk else None      # absent when no sample fell inside the passes
     roof = {"kernel": "up-projection grouped GEMM (SwiGLU epilogue)", "bound": "tensor",
             "achieved": round(up_tf, 1), "peak": burst, "unit": "TFLOP/s",
             "frac": round(up_tf / burst, 4), "traffic": traffic,
@@ -523,7 +523,7 @@ def run_sustained(layer, x, outputs, cfg, alg, args, world, peaks, peak_src, loc
     dn = np.array([r[4].elapsed_time(r[5]) for r in evs])
     peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
     up_tf = alg["up"] / (up.mean() / 1e3) / 1e12
-    mhz = clk["sm_mhz"] if clk else None
+    mhz = clk.get("sm_mhz") if clk else None      # absent when no sample fell inside the passes
     return {"seconds": round(total_ms / 1e3, 3), "steps": n, "ms_per_step": round(total_ms / n, 4),
             "tokens_per_s": round(cfg["T"] * n / (total_ms / 1e3), 1),
             "up_gemm_ms": round(float(up.mean()), 4), "down_gemm_ms": round(float(dn.mean()), 4),

@@ -358,9 +358,9 @@ int run_expert_ffn(const moe_cfg& c, const DevInfo& di, const void* x, const int
         // E4M3: rows of K bytes, 128-byte boxes, swizzled; packed E2M1: rows of
         // K/128 * 80 bytes, 80-byte boxes, not swizzled
         auto wmap = [&](CUtensorMap* m, const void* base, uint64_t rows, int K, const char* what) {
-            return fp4 ? encode_rows(m, base, rows, (uint64_t)(K / 128) * 80, what, 64,
+            return fp4 ? encode_rows(m, base, rows, (uint64_t)(K / 128) * 80, what, lowbit_box_rows(true),
                                      CU_TENSOR_MAP_DATA_TYPE_UINT8, 80, false)
-                       : encode_rows(m, base, rows, (uint64_t)K, what, 64,
+                       : encode_rows(m, base, rows, (uint64_t)K, what, lowbit_box_rows(false),
                                      CU_TENSOR_MAP_DATA_TYPE_UINT8, 128);
         };
         const int up_mode = c.act == MOE_SWIGLU ? kModeSwiglu : kModeGelu;

@@ -29,28 +29,27 @@
 // MMA read), which at 128 B/clock caps the weight stream near the HBM rate;
 // through TMEM it is 2 bytes.
 //
-// One CTA per SM, 384 threads (512 for 4-bit weights, which have two
-// converter warps per lane quadrant); the warps that issue TMA or MMA instructions
+// One CTA per SM, 512 threads; the warps that issue TMA or MMA instructions
 // sit on different schedulers (warp % 4), as issuing them slows the other
 // warps of the scheduler (measured: a converter warp sharing its scheduler
 // with two MMA issuers ran ~2400 clocks behind one sharing with none, and the
 // slowest converter gates both the weight ring and the MMAs):
-//   warp 0      TMA: weight rows (E4M3: 128 bytes of K, 128-byte swizzle,
-//               10-stage ring; E2M1: 80 bytes, 16 stages) into a ring that
-//               the converters release as soon as they hold a stage's codes
-//               in registers;
+//   warp 0      TMA: weight rows (E4M3: 128 bytes of K, 128-byte swizzle;
+//               E2M1: 80 bytes) into a ring of stages of two blocks, 160 KB
+//               in all, that the converters release as soon as they hold a
+//               stage's codes in registers;
 //   warp 1      TMEM owner; TMA: the tile's f16 token rows (128-byte swizzle)
 //               in chunks of up to 24 KB into two buffers, a chunk ahead;
-//   warps 6-9   converters (6-13 for 4-bit), one (two) per TMEM lane
-//               quadrant, thread = weight row: codes -> f16 pairs in
-//               registers, tcgen05.st into the TMEM A buffer of the stage's
-//               block;
-//   last two    MMA issuers, issuer i for blocks i and i + 2 of the tile:
+//   warps 6-13  converters, two sets of one warp per TMEM lane quadrant; set
+//               z takes stage z of each k-block (blocks 2z, 2z + 1), thread
+//               = weight row: codes -> f16 pairs in registers, tcgen05.st
+//               into the TMEM A buffer of each block;
+//   last two    MMA issuers, issuer i for the blocks set i fills:
 //               tcgen05.mma kind::f16 (M=128, N=tokens, K=16), A from the
 //               block's TMEM buffer, B (tokens) from shared memory, into the
 //               block's accumulator.  A thread issues a small MMA only every
-//               ~50-100 clocks and a stage needs 8, so one issuer could not
-//               keep up with the weight stream;
+//               ~50-100 clocks and a block needs 8 per k-block, so one issuer
+//               could not keep up with the weight stream;
 //   warps 2-5   epilogue: row scales, fused activation / gate scale, f16 H
 //               (A operand of the down GEMM) or bf16 slot outputs.  The
 //               scales, biases and token slots of a tile are copied to shared
@@ -91,7 +90,7 @@ namespace {
 constexpr int BK = 128;                        // K values per stage
 constexpr int WROWS = 128;                     // weight rows per block (MMA M, TMEM lanes)
 constexpr int G = 4;                           // weight blocks per tile
-constexpr int NISS = 2;                        // MMA issuers, blocks i, i + NISS, ...
+constexpr int NISS = 2;                        // MMA issuers
 constexpr int TOK = 32;                        // tokens per tile at most (MMA N)
 constexpr int TOK_BOX = 16;                    // token rows per TMA box
 constexpr int TB_BYTES = 24 * 1024;            // token chunk buffer (two of them)
@@ -103,21 +102,38 @@ static_assert(A_COL0 + G * A_COLS <= TMEM_COLS, "tensor memory budget (an A buff
 constexpr int TOKP_WARP = 1;                   // token producer (and TMEM owner)
 constexpr int XCH_LD = 33;
 
-// Weight formats.  Both give a stage 128 values of each weight row (one MMA K
+// Weight formats.  Both give a block 128 values of each weight row (one MMA K
 // range of 128): E4M3 rows of 128 bytes (128-byte swizzle), or packed E2M1
 // rows of 80 bytes (64 code bytes, 8 E4M3 block scales, 8 zero bytes; 80-byte
 // rows put the 16-byte pieces of 8 consecutive rows in 8 different bank
-// groups without a swizzle).  The 4-bit conversion does twice the work per
-// stage (a cvt and a block-scale multiply per pair), so it has two converter
-// warps per TMEM lane quadrant; its ring has more, smaller stages for the same
-// bytes in flight.
+// groups without a swizzle).
+//
+// A ring stage holds SB blocks of one k-block in two boxes of SB * 64 rows
+// (packed E2M1: SB = 2, 20 KB stages).  Each stage costs the producer, the
+// converters and the barriers a fixed number of clocks whatever its size, and
+// with one 10 KB block of E2M1 per stage that cost, not HBM, set the weight
+// stream's pace (measured: a bare TMA ring of 10 KB stages streams 5.2 TB/s,
+// of 20 KB stages 6.6 TB/s, at the same 160 KB in flight).
+//
+// The converters are two sets of four warps; set z converts blocks BPS z ..
+// BPS z + BPS - 1 of every k-block, which MMA issuers BPS z .. consume.  Each set
+// has a ring of its own (RS slots): a slot shared by two consumers that run
+// at their own pace could see its barrier two phases ahead of one of them,
+// where a parity wait cannot tell the phases apart.
 enum { kFmtE4M3 = 0, kFmtE2M1 = 1 };
+constexpr int BPS = G / 2;                     // blocks per converter set
+constexpr int BPI = G / NISS;                  // blocks per MMA issuer
+static_assert(G % 2 == 0 && G % NISS == 0 && BPS % BPI == 0, "two converter sets; issuers within a set");
 template <int FMT>
 struct WF {
     static constexpr int ROW_BYTES = FMT == kFmtE4M3 ? 128 : 80;
-    static constexpr int WQ_BYTES = WROWS * ROW_BYTES;          // one stage of weight rows
-    static constexpr int WSTAGES = FMT == kFmtE4M3 ? 10 : 16;   // weight ring
-    static constexpr int CVT_WARPS = FMT == kFmtE4M3 ? 4 : 8;   // one or two per lane quadrant
+    static constexpr int SB = FMT == kFmtE4M3 ? 1 : 2;          // blocks per ring stage
+    static constexpr int BLK_BYTES = WROWS * ROW_BYTES;         // one block of a k-block
+    static constexpr int WQ_BYTES = SB * BLK_BYTES;             // one ring stage
+    static constexpr int RS = FMT == kFmtE4M3 ? 5 : 4;          // slots per set: 160 KB in flight
+    static constexpr int WSTAGES = 2 * RS;
+    static constexpr int CVT_WARPS = 8;                         // two sets of four, one warp per lane quadrant
+    static_assert(BPS % SB == 0, "a set's blocks are whole stages");
     static constexpr int MMA_WARP0 = 6 + CVT_WARPS;             // first MMA issuer
     static constexpr int NUM_THREADS = (MMA_WARP0 + NISS) * 32;
     static constexpr int OFF_TOK = 0;
@@ -133,11 +149,13 @@ struct WF {
     static constexpr int OFF_OFFS = OFF_START + (kMaxExperts + 2) * 4;
     static constexpr int SMEM_USED = OFF_OFFS + (kMaxExperts + 2) * 4;
     static constexpr int SMEM_BYTES = SMEM_USED + 1024;
-    static_assert(MMA_WARP0 % 4 == 2 && NISS == 2, "issuers on schedulers 2 and 3");
+    static_assert(MMA_WARP0 % 4 == 2 && NISS <= 4, "issuers on different schedulers");
     static_assert(OFF_TOK % 1024 == 0 && TB_BYTES % 1024 == 0, "swizzled token atoms");
     static_assert(OFF_WQ % 1024 == 0 && (FMT != kFmtE4M3 || WQ_BYTES % 1024 == 0),
                   "swizzled weight stages");
-    static_assert(WQ_BYTES % 256 == 0, "128-byte aligned weight boxes");
+    static_assert(BLK_BYTES % 1024 == 0 || FMT != kFmtE4M3, "swizzled second box");
+    static_assert(BLK_BYTES % 256 == 0, "128-byte aligned weight boxes");
+    static_assert(CVT_WARPS == 8, "two converter sets");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 template struct WF<kFmtE4M3>;
@@ -201,12 +219,20 @@ __device__ __forceinline__ Seg decode_seg(const TcFfnArgs& p, const int* s_start
     return t;
 }
 
-// Weight rows of block j of a tile: the first rows of its two 64-row boxes.
-template <int MODE>
-__device__ __forceinline__ int2 block_rows(const TcFfnArgs& p, const Seg& t, int j) {
-    const int u0 = (t.blk0 + j) * Fp8Traits<MODE>::UNITS;
+// First weight rows of the two boxes of stage st of a tile (blocks SB st ..):
+// SwiGLU: the gate rows (W1) and the up rows (W3) of the stage's 128 hidden
+// units; otherwise the stage's blocks one after the other, a box each.
+template <int MODE, int SB>
+__device__ __forceinline__ int2 stage_rows(const TcFfnArgs& p, const Seg& t, int st) {
+    const int u0 = (t.blk0 + st * SB) * Fp8Traits<MODE>::UNITS;
     const int r0 = t.g * p.N + u0;
-    return make_int2(r0, MODE == kModeSwiglu ? r0 : r0 + 64);
+    return make_int2(r0, MODE == kModeSwiglu ? r0 : r0 + SB * 64);
+}
+// Shared-memory row, within its stage, of row r of the stage's block jl.
+template <int MODE, int SB>
+__device__ __forceinline__ int stage_row(int jl, int r) {
+    if (MODE == kModeSwiglu) return r < 64 ? jl * 64 + r : SB * 64 + jl * 64 + (r - 64);
+    return jl * WROWS + r;
 }
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
@@ -318,14 +344,14 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
     if (threadIdx.x == 0) {
         for (int s = 0; s < F::WSTAGES; ++s) {
             ptx::mbar_init(&wfull[s], 1);
-            ptx::mbar_init(&wempty[s], F::CVT_WARPS);
+            ptx::mbar_init(&wempty[s], 4);     // the four warps of one converter set
         }
         for (int s = 0; s < 2; ++s) {
             ptx::mbar_init(&kfull[s], 1);
             ptx::mbar_init(&kempty[s], NISS);
         }
         for (int b = 0; b < G; ++b) {
-            ptx::mbar_init(&cfull[b], F::CVT_WARPS);
+            ptx::mbar_init(&cfull[b], 4);
             ptx::mbar_init(&cempty[b], 1);
         }
         for (int a = 0; a < 2; ++a) {
@@ -419,15 +445,18 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
             int it = 0;
             bool ok = true, held = false;
             const int hold_it = p.hold ? *p.hold - 1 : -1;
+            int used0 = 0, used1 = 0;            // stages issued into each set's ring
             FOR_EACH_SEG(t)
+                const int nst = (t.nblk + F::SB - 1) / F::SB;
                 for (int kb = t.kb0; ok && kb < t.kb1; ++kb)
-                    for (int j = 0; j < t.nblk; ++j, ++it) {
+                    for (int st = 0; st < nst; ++st, ++it) {
                         if (it == hold_it) { ok = false; held = true; break; }   // test hook
-                        const int s = it % F::WSTAGES;
-                        const uint32_t ph = (uint32_t)(it / F::WSTAGES) & 1u;
+                        const int z = st * F::SB / BPS, u = z ? used1++ : used0++;
+                        const int s = z * F::RS + u % F::RS;
+                        const uint32_t ph = (uint32_t)(u / F::RS) & 1u;
                         if (!ptx::mbar_wait_nap(&wempty[s], ph ^ 1u, s_abort, 64)) { ok = false; break; }
                         ptx::mbar_arrive_expect_tx(&wfull[s], F::WQ_BYTES);
-                        const int2 wr = block_rows<MODE>(p, t, j);
+                        const int2 wr = stage_rows<MODE, F::SB>(p, t, st);
                         uint8_t* wq = sWq + s * F::WQ_BYTES;
                         ptx::tma_load_2d(wq, &mapW, &wfull[s], kb * F::ROW_BYTES, wr.x);
                         ptx::tma_load_2d(wq + F::WQ_BYTES / 2, &mapW3, &wfull[s], kb * F::ROW_BYTES, wr.y);
@@ -438,8 +467,11 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
                 *s_abort = 1;
                 raise_error(p.status, MOE_ERR_DEVICE_TIMEOUT);
             }
-            for (int j = (it > F::WSTAGES ? it - F::WSTAGES : 0); j < it; ++j)
-                ptx::mbar_wait(&wfull[j % F::WSTAGES], (uint32_t)(j / F::WSTAGES) & 1u, nullptr);
+            for (int z = 0; z < 2; ++z) {        // the copies still in flight
+                const int n = z ? used1 : used0;
+                for (int j = (n > F::RS ? n - F::RS : 0); j < n; ++j)
+                    ptx::mbar_wait(&wfull[z * F::RS + j % F::RS], (uint32_t)(j / F::RS) & 1u, nullptr);
+            }
         }
     } else if (warp == TOKP_WARP) {
         // ----------------------------------- TMA producer (token chunks)
@@ -478,10 +510,11 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
         }
     } else if (warp >= F::MMA_WARP0) {
         // ------------------------------------------------------- MMA issuers
-        // Issuer mi takes blocks mi, mi + NISS, ... of every tile (their A
-        // buffers and accumulators).  An issuer without a block in a tile
-        // still arrives on the tile's shared barriers (token chunks,
-        // accumulators).
+        // Issuer mi takes blocks BPI mi .. BPI mi + BPI - 1 of every k-block
+        // (their A buffers and accumulators), the blocks converter set mi
+        // fills.  (Four issuers, one per block, measured slower: 18 warps
+        // leave 96 registers a thread, and the up-projections spill.)  An issuer without a block in a tile still
+        // arrives on the tile's shared barriers (token chunks, accumulators).
         const int mi = warp - F::MMA_WARP0;
         if (lane == 0) {
             uint32_t nfill = 0;                 // bit j: parity of block j's fills so far
@@ -491,27 +524,30 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
                 const int acc = tc & 1;
                 const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
                 ++tc;
-                const bool mine = mi < t.nblk;
+                const bool mine = mi * BPI < t.nblk;
                 if (!ptx::mbar_wait_nap(&tempty[acc], aph ^ 1u, s_abort, 64)) { ok = false; break; }
                 ptx::tc_fence_after();
                 const uint32_t idesc = ptx::idesc_f16_f32(WROWS, t.nmma);
-                const int atom = t.nmma * 128;
-                const uint8_t* tb = sTok;
-                int kc = t.kb0;
+                // The issuing thread runs a serial chain on a scheduler shared with
+                // two converter warps, so the k-block loop keeps its scalar work
+                // small: a counter within the token chunk instead of a division
+                // by the chunk length, and B descriptors advanced by a constant
+                // (atoms are 1024-byte aligned; the descriptor's address field
+                // counts 16-byte units).
+                const uint64_t atom_d = (uint64_t)(t.nmma * 128 / 16);
+                uint64_t bd0 = 0;
+                int kk = 0;                                       // k-blocks into the chunk
                 for (int kb = t.kb0; ok && kb < t.kb1; ++kb) {
-                    if ((kb - t.kb0) % CH == 0) {                // next token chunk
+                    if (kk == 0) {                                // next token chunk
                         if (!ptx::mbar_wait_nap(&kfull[cc & 1], (uint32_t)(cc >> 1) & 1u, s_abort, 64)) {
                             ok = false;
                             break;
                         }
-                        tb = sTok + (cc & 1) * TB_BYTES;
-                        kc = kb;
+                        bd0 = ptx::sw128_desc(ptx::smem_u32(sTok + (cc & 1) * TB_BYTES));
                     }
-                    const uint64_t bd0 = ptx::sw128_desc(ptx::smem_u32(tb + (2 * (kb - kc)) * atom));
-                    const uint64_t bd1 =
-                        ptx::sw128_desc(ptx::smem_u32(tb + (2 * (kb - kc) + 1) * atom));
+                    const uint64_t bd1 = bd0 + atom_d;
                     const uint32_t first = kb > t.kb0 ? 1u : 0u;
-                    for (int j = mi; j < t.nblk; j += NISS) {
+                    for (int j = mi * BPI; j < min(mi * BPI + BPI, t.nblk); ++j) {
                         if (!ptx::mbar_wait_nap(&cfull[j], (nfill >> j) & 1u, s_abort, 64)) {
                             ok = false;
                             break;
@@ -531,10 +567,12 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
                         ptx::mma_f16_tmem_a(d_tmem, a_tmem + 56, bd1 + 6, idesc, 1u);
                         ptx::mma_commit(&cempty[j]);
                     }
-                    if (ok && (kb + 1 == t.kb1 || (kb + 1 - t.kb0) % CH == 0)) {   // chunk done
+                    bd0 += 2 * atom_d;
+                    if (ok && (++kk == CH || kb + 1 == t.kb1)) {       // chunk done
                         if (mine) ptx::mma_commit(&kempty[cc & 1]);
                         else ptx::mbar_arrive(&kempty[cc & 1]);
                         ++cc;
+                        kk = 0;
                     }
                 }
                 if (!ok) break;
@@ -550,9 +588,11 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
         }
     } else if (warp >= 6) {
         // -------------------------------------------------------- converters
-        // Thread = weight row r of the warp's TMEM lane quadrant q and part h
-        // (one of CVT_WARPS / 4) of the stage's 128 values; the part's f16
-        // pairs go to TMEM columns (64 / parts) h .. of the block's A buffer.
+        // Thread = weight row r of the warp's TMEM lane quadrant q; the warp
+        // converts all 128 values of its 32 rows of each block of a stage
+        // into that block's A buffer (64 TMEM columns of f16 pairs).  Set z
+        // (four warps) takes the stages of its blocks from its own ring, so
+        // the two sets convert two stages at once.
         //   E4M3: chunk c (16 codes) of the row sits at c ^ (r & 7) (128-byte
         //   swizzle: 8 consecutive rows hit 8 different bank groups); a code
         //   pair -> an f16 pair (exact).
@@ -560,90 +600,94 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
         //   low, high nibble of byte i) and 8 E4M3 scales, one per 16 values;
         //   a code byte -> an f16 pair, times its block scale as an f16 pair
         //   (exact: every E2M1 value times an E4M3 value is an f16 value).
-        constexpr int PARTS = F::CVT_WARPS / 4;
-        constexpr int COLS = 64 / PARTS;                     // TMEM columns per part
-        static_assert(FMT == kFmtE4M3 || PARTS == 2, "an E2M1 part is 4 pieces' worth of scales");
-        const int q = warp & 3, h = (warp - 6) >> 2;
+        constexpr int SB = F::SB;
+        const int q = warp & 3, z = (warp - 6) >> 2;
         const int r = q * 32 + lane;
-        const uint32_t a_lane =
-            tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(A_COL0 + COLS * h);
-        int it = 0;
+        const uint32_t a_lane = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)A_COL0;
+        int u = 0;                               // stages taken from this set's ring
         uint32_t nfill = 0;                      // bit j: parity of A buffer j's fills so far
         bool ok = true;
         FOR_EACH_SEG(t)
+            const int nst = (t.nblk + SB - 1) / SB;
             for (int kb = t.kb0; ok && kb < t.kb1; ++kb)
-                for (int j = 0; j < t.nblk; ++j, ++it) {
-                    const int s = it % F::WSTAGES, b = j;
-                    const uint32_t ph = (uint32_t)(it / F::WSTAGES) & 1u;
-                    const uint32_t bph = (nfill >> b) & 1u;
-                    nfill ^= 1u << b;
+                for (int st = z * BPS / SB; ok && st < min(nst, (z + 1) * BPS / SB); ++st, ++u) {
+                    const int s = z * F::RS + u % F::RS;
+                    const uint32_t ph = (uint32_t)(u / F::RS) & 1u;
                     if (!__all_sync(0xffffffffu, ptx::mbar_wait(&wfull[s], ph, s_abort))) {
                         ok = false;
                         break;
                     }
-                    const uint8_t* src = sWq + s * F::WQ_BYTES + r * F::ROW_BYTES;
-                    constexpr int NQ = FMT == kFmtE4M3 ? 8 / PARTS : 4 / PARTS;
-                    uint4 qv[NQ];
-                    uint32_t sc = 0;                             // E2M1: the part's block scales
-                    if constexpr (FMT == kFmtE4M3) {
+                    const int jn = min(SB, t.nblk - st * SB);    // blocks of the stage
+                    for (int jl = 0; jl < jn; ++jl) {
+                        const int b = st * SB + jl;
+                        const uint32_t bph = (nfill >> b) & 1u;
+                        nfill ^= 1u << b;
+                        const uint8_t* src =
+                            sWq + s * F::WQ_BYTES + stage_row<MODE, SB>(jl, r) * F::ROW_BYTES;
+                        constexpr int NQ = FMT == kFmtE4M3 ? 8 : 4;   // 16-byte code chunks
+                        uint4 qv[NQ];
+                        uint2 sc = make_uint2(0u, 0u);                // E2M1: the 8 block scales
+                        if constexpr (FMT == kFmtE4M3) {
 #pragma unroll
-                        for (int i = 0; i < NQ; ++i)
-                            qv[i] = *reinterpret_cast<const uint4*>(
-                                src + (((NQ * h + i) ^ (r & 7)) << 4));
-                    } else {
+                            for (int i = 0; i < NQ; ++i)
+                                qv[i] = *reinterpret_cast<const uint4*>(src + ((i ^ (r & 7)) << 4));
+                        } else {
 #pragma unroll
-                        for (int i = 0; i < NQ; ++i)
-                            qv[i] = *reinterpret_cast<const uint4*>(src + (NQ * h + i) * 16);
-                        sc = *reinterpret_cast<const uint32_t*>(src + 64 + 4 * h);
-                    }
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(&wempty[s]);     // codes are in registers
-                    if (!__all_sync(0xffffffffu, ptx::mbar_wait(&cempty[b], bph ^ 1u, s_abort))) {
-                        ok = false;
-                        break;
-                    }
-                    ptx::tc_fence_after();
-                    if constexpr (FMT == kFmtE4M3) {
-#pragma unroll
-                        for (int hh = 0; hh < NQ / 2; ++hh) {     // 16 columns at a time
-                            uint32_t wv[16];
-#pragma unroll
-                            for (int i = 0; i < 2; ++i) {
-                                const uint4 c = qv[2 * hh + i];
-                                e4m3x4_to_f16x4(c.x, wv[8 * i + 0], wv[8 * i + 1]);
-                                e4m3x4_to_f16x4(c.y, wv[8 * i + 2], wv[8 * i + 3]);
-                                e4m3x4_to_f16x4(c.z, wv[8 * i + 4], wv[8 * i + 5]);
-                                e4m3x4_to_f16x4(c.w, wv[8 * i + 6], wv[8 * i + 7]);
-                            }
-                            ptx::tmem_st16(a_lane + (uint32_t)(b * A_COLS + hh * 16), wv);
+                            for (int i = 0; i < NQ; ++i)
+                                qv[i] = *reinterpret_cast<const uint4*>(src + i * 16);
+                            sc = *reinterpret_cast<const uint2*>(src + 64);
                         }
-                    } else {
-                        // 16 bytes = 32 values = two blocks of 16 per piece
-                        const uint32_t s01 = ptx::cvt_e4m3x2_f16x2((uint16_t)(sc & 0xffffu));
-                        const uint32_t s23 = ptx::cvt_e4m3x2_f16x2((uint16_t)(sc >> 16));
-#pragma unroll
-                        for (int i = 0; i < NQ; ++i) {              // 16 columns per piece
-                            const uint32_t pair = i < 1 ? s01 : s23;
-                            const uint32_t b0 = __byte_perm(pair, 0, 0x1010);   // low half, twice
-                            const uint32_t b1 = __byte_perm(pair, 0, 0x3232);   // high half, twice
-                            const uint32_t words[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
-                            uint32_t wv[16];
-#pragma unroll
-                            for (int w = 0; w < 4; ++w) {
-                                const uint32_t bs = w < 2 ? b0 : b1;
-                                uint32_t c[4];
-                                ptx::cvt_e2m1x8_f16x8(words[w], c);
-#pragma unroll
-                                for (int by = 0; by < 4; ++by)
-                                    wv[4 * w + by] = ptx::mul_f16x2(c[by], bs);
-                            }
-                            ptx::tmem_st16(a_lane + (uint32_t)(b * A_COLS + i * 16), wv);
+                        if (jl == jn - 1) {                      // the stage's codes are in registers
+                            __syncwarp();
+                            if (lane == 0) ptx::mbar_arrive(&wempty[s]);
                         }
+                        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&cempty[b], bph ^ 1u, s_abort))) {
+                            ok = false;
+                            break;
+                        }
+                        ptx::tc_fence_after();
+                        if constexpr (FMT == kFmtE4M3) {
+#pragma unroll
+                            for (int hh = 0; hh < NQ / 2; ++hh) {     // 16 columns at a time
+                                uint32_t wv[16];
+#pragma unroll
+                                for (int i = 0; i < 2; ++i) {
+                                    const uint4 c = qv[2 * hh + i];
+                                    e4m3x4_to_f16x4(c.x, wv[8 * i + 0], wv[8 * i + 1]);
+                                    e4m3x4_to_f16x4(c.y, wv[8 * i + 2], wv[8 * i + 3]);
+                                    e4m3x4_to_f16x4(c.z, wv[8 * i + 4], wv[8 * i + 5]);
+                                    e4m3x4_to_f16x4(c.w, wv[8 * i + 6], wv[8 * i + 7]);
+                                }
+                                ptx::tmem_st16(a_lane + (uint32_t)(b * A_COLS + hh * 16), wv);
+                            }
+                        } else {
+                            // 16 bytes = 32 values = two blocks of 16 per piece
+#pragma unroll
+                            for (int i = 0; i < NQ; ++i) {              // 16 columns per piece
+                                const uint32_t sw = i < 2 ? sc.x : sc.y;
+                                const uint32_t pair = ptx::cvt_e4m3x2_f16x2(
+                                    (uint16_t)((i & 1) ? (sw >> 16) : (sw & 0xffffu)));
+                                const uint32_t b0 = __byte_perm(pair, 0, 0x1010);   // low half, twice
+                                const uint32_t b1 = __byte_perm(pair, 0, 0x3232);   // high half, twice
+                                const uint32_t words[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
+                                uint32_t wv[16];
+#pragma unroll
+                                for (int w = 0; w < 4; ++w) {
+                                    const uint32_t bs = w < 2 ? b0 : b1;
+                                    uint32_t c[4];
+                                    ptx::cvt_e2m1x8_f16x8(words[w], c);
+#pragma unroll
+                                    for (int by = 0; by < 4; ++by)
+                                        wv[4 * w + by] = ptx::mul_f16x2(c[by], bs);
+                                }
+                                ptx::tmem_st16(a_lane + (uint32_t)(b * A_COLS + i * 16), wv);
+                            }
+                        }
+                        ptx::tmem_wait_st();                  // the block's stores, then signal
+                        ptx::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) ptx::mbar_arrive(&cfull[b]);
                     }
-                    ptx::tmem_wait_st();                  // the stage's stores, then signal
-                    ptx::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(&cfull[b]);
                 }
             if (!ok) break;
         }
@@ -775,6 +819,10 @@ cudaError_t launch_fmt(int mode, const CUtensorMap* maps, const TcFfnArgs& p, in
     if (mode == kModeSwiglu) return launch_one<kModeSwiglu, FMT>(maps, p, num_sms, st);
     if (mode == kModeGelu) return launch_one<kModeGelu, FMT>(maps, p, num_sms, st);
     return launch_one<kModeDown, FMT>(maps, p, num_sms, st);
+}
+
+int lowbit_box_rows(bool fp4) {
+    return fp4 ? WF<kFmtE2M1>::SB * 64 : WF<kFmtE4M3>::SB * 64;
 }
 
 cudaError_t launch_ffn_fp8(int mode, const CUtensorMap* maps, const TcFfnArgs& p, int num_sms,

@@ -154,12 +154,14 @@ cudaError_t launch_ffn_tc(int mode, const CUtensorMap* maps, const TcFfnArgs& p,
 // at most kFp8MaxGrid CTAs (its partial-sum slots: 2 per CTA of 4 weight blocks
 // x 128 rows x 32 tokens fp32, and one ticket per CTA)
 // maps: X (f16 token rows, box 64 x 16), W and W3 (E4M3 rows, box 128 bytes x
-// 64 rows; W3 = W for GELU / down), all with the 128-byte swizzle
+// lowbit_box_rows(false) rows; W3 = W for GELU / down), all with the 128-byte swizzle
 constexpr int kFp8MaxGrid = 160;
 constexpr size_t kFp8SplitBytes = (size_t)2 * kFp8MaxGrid * 4 * 128 * 32 * 4;
 // fp4: packed E2M1 weights (rows of 80-byte chunks: 64 code bytes, 8 E4M3 block
-// scales, 8 zero bytes per 128 values; weight maps with box 80 bytes x 64 rows,
-// no swizzle) instead of E4M3
+// scales, 8 zero bytes per 128 values; weight maps with box 80 bytes x
+// lowbit_box_rows(true) rows, no swizzle) instead of E4M3
+// rows of one TMA box of low-bit weight rows (a ring stage is two boxes)
+int lowbit_box_rows(bool fp4);
 cudaError_t launch_ffn_fp8(int mode, const CUtensorMap* maps, const TcFfnArgs& p, int num_sms,
                            cudaStream_t st, bool fp4 = false);
 // ffn_tc2.cu: the same on CTA pairs (cta_group::2), 256-row tiles; same maps

@@ -162,11 +162,12 @@ def test_lookback_wait_times_out_and_reports():
 
 @pytest.mark.parametrize("kern,low,hold", [("tc1", None, 0), ("tc1", None, 5), ("pair", None, 0),
                                            ("pair", None, 5), ("swap", None, 0), ("swap", None, 5),
-                                           ("auto", "fp8", 0)])
+                                           ("auto", "fp8", 0), ("auto", "fp8", 3),
+                                           ("auto", "fp4", 3)])
 def test_gemm_wait_times_out_and_reports(kern, low, hold):
     """Failure path of the expert GEMMs' bounded waits: with the up-projection's
     weight producer stopped before ring iteration `hold` (the copy never
-    arrives), the MMA issuer (FP8: the converters) gives up after about a
+    arrives), the MMA issuer (low-bit weights: the converters) gives up after about a
     second, the device status reads MOE_ERR_DEVICE_TIMEOUT, the kernel drains
     its own copies and MMAs, frees its tensor memory and returns, and a clean
     call on a fresh workspace reproduces the earlier output bit for bit.
@@ -178,6 +179,9 @@ def test_gemm_wait_times_out_and_reports(kern, low, hold):
     inp = workloads.make_inputs(cfg, device="cuda")
     if low == "fp8":
         inp = workloads.quantize_experts_fp8(inp)
+        cfg = inp["cfg"]
+    elif low == "fp4":
+        inp = workloads.quantize_experts_fp4(inp)
         cfg = inp["cfg"]
     layer = binding.MoeLayer(cfg, inp)
     ref = layer.forward(inp["x"])["y"].clone()
