@@ -99,7 +99,7 @@ gemm_strided_simt(int M, int N, int K, const TA* __restrict__ A, long long sam, 
             As[c][r] = (gm < M && gk < K) ? Elem<TA>::load(A + gm * sam + gk * sak) : 0.f;
             Bs[c][r] = (gn < N && gk < K) ? Elem<TB>::load(B + gk * sbk + gn * sbn) : 0.f;
         }
-        __syncthreads();
+        block_sync();
 #pragma unroll
         for (int kk = 0; kk < BK; ++kk) {
             const float4 a = *reinterpret_cast<const float4*>(&As[kk][ty * 4]);
@@ -111,7 +111,7 @@ gemm_strided_simt(int M, int N, int K, const TA* __restrict__ A, long long sam, 
 #pragma unroll
                 for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
         }
-        __syncthreads();
+        block_sync();
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {

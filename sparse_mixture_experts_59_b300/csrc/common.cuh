@@ -9,6 +9,35 @@
 
 namespace moe {
 
+// Block-wide barrier.  Each warp reconverges first: bar.sync counts a warp's
+// arrival as the whole warp, so in code where the lanes of a warp can reach
+// the barrier apart (a role loop run by lane 0, per-lane spin waits) the
+// lanes that arrive first would count the warp as arrived, and the barrier
+// could pass while other warps still work.
+__device__ __forceinline__ void block_sync() {
+    __syncwarp();
+    __syncthreads();
+}
+
+// Loads, at L2, of values that other CTAs published before a ticket or flag
+// this thread has already observed.  Volatile with a memory clobber: __ldcg's
+// asm is neither, and nothing would then stop the compiler from moving it
+// above the synchronisation that makes the values valid.
+__device__ __forceinline__ float ld_cg(const float* p) {
+    float v;
+    asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ float4 ld_cg(const float4* p) {
+    float4 v;
+    asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p)
+                 : "memory");
+    return v;
+}
+
+
 // ---------------------------------------------------------------- limits
 constexpr int kMaxExperts = 256;   // one dispatch thread per expert
 constexpr int kMaxTopK = 8;
@@ -100,7 +129,7 @@ __device__ __forceinline__ float silu(float z) {
 // tiles(g) = ceil(rows(g) / tile_rows) * ntiles_n(g), where rows(g) comes from
 // offsets for routed groups g < E and is `shared_rows` for g == E (when
 // shared_rows > 0).  Must be called by all threads of the block; ends with a
-// __syncthreads.  Uses warp 0 for the scan.
+// block barrier.  Uses warp 0 for the scan.
 __device__ __forceinline__ void group_tile_prefix(const int* __restrict__ offsets, int E,
                                                   int shared_rows, int tile_rows, int nt_routed,
                                                   int nt_shared, int* s_start) {
@@ -128,7 +157,7 @@ __device__ __forceinline__ void group_tile_prefix(const int* __restrict__ offset
         }
         if (lane == 0) s_start[G] = carry;
     }
-    __syncthreads();
+    block_sync();
 }
 
 // Group g holding linear tile index `tile` (s_start ascending, G groups).

@@ -56,7 +56,7 @@ dispatch_rank_kernel(const int* __restrict__ topk_idx, int A, int Ttok, int E,
     pdl_trigger();
     if (tid == 0) s_bid = atomicAdd(ctrl + kCtrlDispatchTicket, 1);
     if (tid < E) s_run[tid] = 0;
-    __syncthreads();
+    block_sync();
     const int bid = s_bid;
     const int nblk = gridDim.x;
     const int base = bid * kDspChunk;
@@ -77,11 +77,11 @@ dispatch_rank_kernel(const int* __restrict__ topk_idx, int A, int Ttok, int E,
         const int buf = it & 1;
 #pragma unroll
         for (int w = 0; w < kDspWarps; ++w) s_cnt[buf][w][tid] = 0;
-        __syncthreads();
+        block_sync();
         const unsigned peers = __match_any_sync(0xffffffffu, e);
         const int in_warp = __popc(peers & lt_mask);
         if (e >= 0 && lane == __ffs(peers) - 1) s_cnt[buf][warp][e] = __popc(peers);
-        __syncthreads();
+        block_sync();
         if (tid < E) {                       // exclusive scan over warps, per expert
             int run = s_run[tid];
 #pragma unroll
@@ -92,7 +92,7 @@ dispatch_rank_kernel(const int* __restrict__ topk_idx, int A, int Ttok, int E,
             }
             s_run[tid] = run;
         }
-        __syncthreads();
+        block_sync();
         my_e[it] = e;
         my_rank[it] = (e >= 0) ? s_cnt[buf][warp][e] + in_warp : -1;
     }
@@ -131,7 +131,7 @@ dispatch_rank_kernel(const int* __restrict__ topk_idx, int A, int Ttok, int E,
             if (!hold) st_release_u32(mine, kFlagPrefix | ((excl + agg) & kValueMask));
         }
     }
-    __syncthreads();
+    block_sync();
 #pragma unroll
     for (int it = 0; it < kDspItems; ++it) {
         const int a = base + it * kDspThreads + tid;
@@ -140,9 +140,9 @@ dispatch_rank_kernel(const int* __restrict__ topk_idx, int A, int Ttok, int E,
 
     // the last block to finish produces the totals
     __threadfence();
-    __syncthreads();
+    block_sync();
     if (tid == 0) s_last = (atomicAdd(ctrl + kCtrlDispatchDone, 1) == nblk - 1);
-    __syncthreads();
+    block_sync();
     if (!s_last) return;
     __threadfence();
     int total = 0, kept = 0;
@@ -162,12 +162,12 @@ dispatch_rank_kernel(const int* __restrict__ topk_idx, int A, int Ttok, int E,
     }
     __shared__ int s_wsum[kDspWarps];
     if (lane == 31) s_wsum[warp] = incl;
-    __syncthreads();
+    block_sync();
     int wbase = 0;
     for (int w = 0; w < warp; ++w) wbase += s_wsum[w];
     if (tid < E) offsets[tid] = wbase + incl - kept;
     if (tid == E - 1) offsets[E] = wbase + incl;
-    __syncthreads();
+    block_sync();
     if (tid == 0) {
         int R = 0;
         for (int w = 0; w < kDspWarps; ++w) R += s_wsum[w];

@@ -235,7 +235,15 @@ __device__ __forceinline__ int stage_row(int jl, int r) {
     return jl * WROWS + r;
 }
 
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Named barrier of the four epilogue warps.  Each warp reconverges first:
+// bar.sync counts a warp's arrival as the whole warp, and one lane may still
+// be in a branch of its own (the ticket of a shared tile): arriving without
+// it would release the barrier early and pair the warps' later barriers up
+// out of step.
+__device__ __forceinline__ void epi_bar() {
+    __syncwarp();
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+}
 
 // Epilogue of one block's accumulator (tokens 0..31) for the calling thread's
 // weight row `row`; v holds the sums over the unscaled codes.
@@ -378,7 +386,7 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
     // by the epilogue, after MMAs that consumed waited-for tokens.
     pdl_trigger();
     for (int i = threadIdx.x; i <= p.E; i += F::NUM_THREADS) s_off[i] = p.offsets[i];
-    __syncthreads();
+    block_sync();
     const int nwb = (p.N + Fp8Traits<MODE>::UNITS - 1) / Fp8Traits<MODE>::UNITS;
     if (warp == 0) {            // longest segment: sizes the token chunks
         int m = 0;
@@ -389,7 +397,7 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
     }
     group_tile_prefix(s_off, p.E, 0, TOK, (nwb + G - 1) / G, 0, s_start);
     ptx::tc_fence_before();
-    __syncthreads();
+    block_sync();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *s_tmem;
     const int grid = (int)gridDim.x;
@@ -771,19 +779,45 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
             epi_bar();
             if (!*s_last) continue;
             __threadfence();
+            // The parts are added in CTA order (the result repeats exactly).
+            // The loads of up to four parts and eight columns are issued
+            // together: these L2 round trips trail the kernel, and one at a
+            // time per part made the last tiles of a decode-sized down
+            // projection finish 15-25 us after the others.
             for (int j = 0; j < t.nblk; ++j) {
                 float v[32];
 #pragma unroll
                 for (int c = 0; c < 32; ++c) v[c] = 0.f;
-                for (int cta = t.c_first; cta <= t.c_last; ++cta) {
-                    const long long s0 = cta_start(W, grid, cta);
-                    if (s0 == cta_start(W, grid, cta + 1)) continue;        // no work there
-                    const int sl = (t.tile == (int)(s0 / nk)) ? 0 : 1;
-                    const float* src =
-                        p.split_part + ((size_t)cta * 2 + sl) * G * slot_floats + j * slot_floats;
+                for (int cta0 = t.c_first; cta0 <= t.c_last; cta0 += 4) {
+                    const float* src[4];
 #pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        if (c < t.ntok) v[c] += __ldcg(src + (size_t)c * WROWS + row);
+                    for (int q = 0; q < 4; ++q) {
+                        const int cta = cta0 + q;
+                        src[q] = nullptr;
+                        if (cta > t.c_last) continue;
+                        const long long s0 = cta_start(W, grid, cta);
+                        if (s0 == cta_start(W, grid, cta + 1)) continue;    // no work there
+                        const int sl = (t.tile == (int)(s0 / nk)) ? 0 : 1;
+                        src[q] = p.split_part + ((size_t)cta * 2 + sl) * G * slot_floats +
+                                 j * slot_floats + row;
+                    }
+#pragma unroll
+                    for (int c0 = 0; c0 < 32; c0 += 8) {
+                        if (c0 >= t.ntok) break;
+                        float x[4][8];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                x[q][i] = (src[q] && c0 + i < t.ntok)
+                                              ? ld_cg(src[q] + (size_t)(c0 + i) * WROWS) : 0.f;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            if (!src[q]) continue;
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) v[c0 + i] += x[q][i];
+                        }
+                    }
                 }
                 finish_block<MODE>(p, t, j, row, v, s_xch, s_pre, tok_a, tok_w);
             }
@@ -791,8 +825,10 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
     }
 #undef FOR_EACH_SEG
 
+    // every role done (lane 0 of several warps ran a role loop of its own:
+    // block_sync reconverges each warp before the barrier), then free TMEM
     ptx::tc_fence_before();
-    __syncthreads();
+    block_sync();
     if (warp == 1) {
         __syncwarp();
         ptx::tc_fence_after();

@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(256) ffn_simt_kernel(SimtFfnArgs p) {
             Bs[c][rr] = (gn < N && gc < K) ? B[(size_t)gn * K + gc] : 0.f;
             if (MODE == kModeSwiglu) B2s[c][rr] = (gn < N && gc < K) ? B2[(size_t)gn * K + gc] : 0.f;
         }
-        __syncthreads();
+        block_sync();
 #pragma unroll
         for (int kk = 0; kk < kSimtBK; ++kk) {
             const float4 a = *reinterpret_cast<const float4*>(&As[kk][ty * 4]);
@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(256) ffn_simt_kernel(SimtFfnArgs p) {
                     for (int j = 0; j < 4; ++j) acc2[i][j] = fmaf(av[i], b2v[j], acc2[i][j]);
             }
         }
-        __syncthreads();
+        block_sync();
     }
 
 #pragma unroll

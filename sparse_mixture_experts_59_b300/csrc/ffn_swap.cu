@@ -96,7 +96,15 @@ __device__ __forceinline__ STile decode(const TcFfnArgs& p, const int* s_start, 
     return t;
 }
 
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Named barrier of the four epilogue warps.  Each warp reconverges first:
+// bar.sync counts a warp's arrival as the whole warp, and one lane may still
+// be in a branch of its own (the ticket of a shared tile): arriving without
+// it would release the barrier early and pair the warps' later barriers up
+// out of step.
+__device__ __forceinline__ void epi_bar() {
+    __syncwarp();
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+}
 
 template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -338,8 +346,7 @@ ffn_swap_kernel(const __grid_constant__ CUtensorMap mapW, const __grid_constant_
     }
 
     ptx::tc_fence_before();
-    __syncthreads();
-    __syncwarp();
+    block_sync();
     ptx::cluster_sync();
     if (warp == 1) {
         __syncwarp();

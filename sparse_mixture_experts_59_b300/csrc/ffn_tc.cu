@@ -114,7 +114,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
     const int nt_s = p.rows_sh > 0 ? (p.N_sh + BN_OUT - 1) / BN_OUT : 0;
     group_tile_prefix(p.offsets, p.E, p.rows_sh, BM, nt_r, nt_s, s_start);
     ptx::tc_fence_before();
-    __syncthreads();
+    block_sync();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *s_tmem;
     const int G = p.E + (p.rows_sh > 0 ? 1 : 0);
@@ -213,9 +213,10 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
         }
     }
 
-    // teardown: all roles done (or aborted); free TMEM
+    // teardown: all roles done (or aborted; block_sync reconverges the warps
+    // whose lane 0 ran a role loop); free TMEM
     ptx::tc_fence_before();
-    __syncthreads();
+    block_sync();
     if (warp == 1) {
         __syncwarp();
         ptx::tc_fence_after();

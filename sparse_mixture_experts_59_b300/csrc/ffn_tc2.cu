@@ -218,8 +218,7 @@ ffn_tc2_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
     // teardown: both CTAs finished (no remote arrive still targets either),
     // then each frees its half of the pair's TMEM allocation
     ptx::tc_fence_before();
-    __syncthreads();
-    __syncwarp();
+    block_sync();
     ptx::cluster_sync();
     if (warp == 1) {
         __syncwarp();

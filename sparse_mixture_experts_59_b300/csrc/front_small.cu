@@ -108,7 +108,7 @@ front_small_kernel(const Tin* __restrict__ x, const Tin* __restrict__ Wr,
                     for (int q = 0; q < VEC; ++q) dst[q] = 0.f;
                 }
             }
-            __syncthreads();
+            block_sync();
 #pragma unroll
             for (int j = 0; j < kMaxOut; ++j) {
                 const int o = tid + j * kThreads;
@@ -131,7 +131,7 @@ front_small_kernel(const Tin* __restrict__ x, const Tin* __restrict__ Wr,
                     acc[j] += (s4[0] + s4[1]) + (s4[2] + s4[3]);
                 }
             }
-            __syncthreads();
+            block_sync();
         }
         float* mine = part + (size_t)blockIdx.x * TE;
 #pragma unroll
@@ -142,13 +142,13 @@ front_small_kernel(const Tin* __restrict__ x, const Tin* __restrict__ Wr,
     }
     // the block's partials, then one fence and the ticket (the fence of the
     // thread that takes the ticket orders the whole block's writes before it)
-    __syncthreads();
+    block_sync();
     if (tid == 0) {
         __threadfence();
         s_last = (atomicAdd(ticket, 1) == (int)gridDim.x - 1);
         if (s_last) __threadfence();
     }
-    __syncthreads();
+    block_sync();
     if (!s_last) return;
 
     // ---------------------------------------------- phase 2 (last CTA only)
@@ -167,7 +167,7 @@ front_small_kernel(const Tin* __restrict__ x, const Tin* __restrict__ Wr,
         float v32[kMaxSplits];
 #pragma unroll
         for (int a = 0; a < kMaxSplits; ++a)
-            v32[a] = a < S ? __ldcg(part + (size_t)a * TE + o) : 0.f;
+            v32[a] = a < S ? ld_cg(part + (size_t)a * TE + o) : 0.f;
 #pragma unroll
         for (int w = kMaxSplits / 2; w > 0; w >>= 1)
 #pragma unroll
@@ -177,7 +177,7 @@ front_small_kernel(const Tin* __restrict__ x, const Tin* __restrict__ Wr,
         s_logit[o] = v;
         logits[o] = v;
     }
-    __syncthreads();
+    block_sync();
 
     // routing: one warp per token
     for (int t = warp; t < Ttok; t += kWarps) {
@@ -200,7 +200,7 @@ front_small_kernel(const Tin* __restrict__ x, const Tin* __restrict__ Wr,
             s_idx[t * k + lane] = my_idx;
         }
     }
-    __syncthreads();
+    block_sync();
 
     // P_e (four token chains, added in a fixed order), then per-expert ranks
     // in flattened order
@@ -227,7 +227,7 @@ front_small_kernel(const Tin* __restrict__ x, const Tin* __restrict__ Wr,
             if (s_idx[a] == tid) s_rank[a] = c++;
         s_cnt[tid] = c;
     }
-    __syncthreads();
+    block_sync();
 
     // capacity, counts and offsets (exclusive scan of the kept counts)
     int total = 0, kept = 0;
@@ -244,7 +244,7 @@ front_small_kernel(const Tin* __restrict__ x, const Tin* __restrict__ Wr,
         if (lane >= o) incl += n;
     }
     if (lane == 31) s_wsum[warp] = incl;
-    __syncthreads();
+    block_sync();
     int wbase = 0;
     for (int w = 0; w < warp; ++w) wbase += s_wsum[w];
     if (tid < E) {
@@ -252,7 +252,7 @@ front_small_kernel(const Tin* __restrict__ x, const Tin* __restrict__ Wr,
         offsets[tid] = wbase + incl - kept;
     }
     if (tid == E - 1) offsets[E] = wbase + incl;
-    __syncthreads();
+    block_sync();
 
     // dest / perm_src / drop mask
     for (int a = tid; a < A; a += kThreads) {

@@ -45,7 +45,7 @@ router_logits_simt(const T* __restrict__ x, const T* __restrict__ Wr,
             const int ge = n0 + r;
             Ws[c][r] = (ge < E && gc < d) ? Elem<T>::load(Wr + (size_t)ge * d + gc) : 0.f;
         }
-        __syncthreads();
+        block_sync();
 #pragma unroll
         for (int kk = 0; kk < BK; ++kk) {
             const float4 a = *reinterpret_cast<const float4*>(&Xs[kk][ty * 4]);
@@ -57,7 +57,7 @@ router_logits_simt(const T* __restrict__ x, const T* __restrict__ Wr,
 #pragma unroll
                 for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
         }
-        __syncthreads();
+        block_sync();
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -137,7 +137,7 @@ router_topk_kernel(const float* part, int nsplit, const float* __restrict__ bias
         }
     }
     if (!want_p) return;
-    __syncthreads();
+    block_sync();
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         float s = 0.f;
 #pragma unroll
@@ -145,9 +145,9 @@ router_topk_kernel(const float* part, int nsplit, const float* __restrict__ bias
         prob_part[(size_t)blockIdx.x * E + e] = s;
     }
     __threadfence();
-    __syncthreads();
+    block_sync();
     if (threadIdx.x == 0) s_last = (atomicAdd(done_counter, 1) == (int)gridDim.x - 1);
-    __syncthreads();
+    block_sync();
     if (!s_last) return;
     __threadfence();
     // column sums of prob_part[nblocks][E], in a fixed order so that the
@@ -172,12 +172,12 @@ router_topk_kernel(const float* part, int nsplit, const float* __restrict__ bias
             for (; b + 7 * G < nb; b += 8 * G) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const float4 v = __ldcg(src + (size_t)(b + j * G) * C);
+                    const float4 v = ld_cg(src + (size_t)(b + j * G) * C);
                     a[j].x += v.x; a[j].y += v.y; a[j].z += v.z; a[j].w += v.w;
                 }
             }
             for (; b < nb; b += G) {
-                const float4 v = __ldcg(src + (size_t)b * C);
+                const float4 v = ld_cg(src + (size_t)b * C);
                 a[0].x += v.x; a[0].y += v.y; a[0].z += v.z; a[0].w += v.w;
             }
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -196,15 +196,15 @@ router_topk_kernel(const float* part, int nsplit, const float* __restrict__ bias
             int b = g;
             for (; b + 7 * G < nb; b += 8 * G)
 #pragma unroll
-                for (int j = 0; j < 8; ++j) a8[j] += __ldcg(prob_part + (size_t)(b + j * G) * E + e);
-            for (; b < nb; b += G) a8[0] += __ldcg(prob_part + (size_t)b * E + e);
+                for (int j = 0; j < 8; ++j) a8[j] += ld_cg(prob_part + (size_t)(b + j * G) * E + e);
+            for (; b < nb; b += G) a8[0] += ld_cg(prob_part + (size_t)b * E + e);
             float acc = 0.f;
 #pragma unroll
             for (int j = 0; j < 8; ++j) acc += a8[j];
             s_col[g * E + e] = acc;
         }
     }
-    __syncthreads();
+    block_sync();
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         float acc = 0.f;
         for (int g = 0; g < G; ++g) acc += s_col[g * E + e];

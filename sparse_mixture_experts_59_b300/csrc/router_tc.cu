@@ -68,7 +68,7 @@ router_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constan
         ptx::tmem_relinquish();
     }
     ptx::tc_fence_before();
-    __syncthreads();
+    block_sync();
     ptx::tc_fence_after();
     const uint32_t tmem = *s_tmem;
     pdl_wait();       // x may come from the preceding kernel; part is reused across calls
@@ -146,7 +146,7 @@ router_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constan
         if (lane == 0) raise_error(status, MOE_ERR_DEVICE_TIMEOUT);
     }
     ptx::tc_fence_before();
-    __syncthreads();
+    block_sync();
     if (warp == 1) {
         __syncwarp();
         ptx::tc_fence_after();
