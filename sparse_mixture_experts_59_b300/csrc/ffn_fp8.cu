@@ -143,7 +143,7 @@ struct WF {
     static constexpr int OFF_TOKA = OFF_PRE + 2 * G * WROWS * 4;
     static constexpr int OFF_TOKW = OFF_TOKA + 2 * TOK * 4;     // token slots and weights, 2 buffers
     static constexpr int OFF_BAR = OFF_TOKW + 2 * TOK * 4;
-    static constexpr int NUM_BARS = 2 * WSTAGES + 2 + 2 + 2 * G + 2 + 2 + NISS;
+    static constexpr int NUM_BARS = 2 * WSTAGES + 2 + 2 + 2 * G + 2 + 2 + NISS + 1;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_START = OFF_MISC + 32;
     static constexpr int OFF_OFFS = OFF_START + (kMaxExperts + 2) * 4;
@@ -340,6 +340,7 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
     uint64_t* tfull = cempty + G;                // the issuers' accumulators complete
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;                // per issuer
+    uint64_t* endbar = drain + NISS;             // teardown: every thread
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + F::OFF_MISC);
     volatile int* s_abort = reinterpret_cast<volatile int*>(smem + F::OFF_MISC + 4);
     volatile int* s_go = reinterpret_cast<volatile int*>(smem + F::OFF_MISC + 8);
@@ -367,6 +368,7 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
             ptx::mbar_init(&tempty[a], 128);
         }
         for (int j = 0; j < NISS; ++j) ptx::mbar_init(&drain[j], 1);
+        ptx::mbar_init(endbar, F::NUM_THREADS);
         *s_abort = 0;
         ptx::fence_mbarrier_init();
         ptx::prefetch_tensormap(&mapX);
@@ -825,10 +827,9 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
     }
 #undef FOR_EACH_SEG
 
-    // every role done (lane 0 of several warps ran a role loop of its own:
-    // block_sync reconverges each warp before the barrier), then free TMEM
+    // every role done, then free TMEM
     ptx::tc_fence_before();
-    block_sync();
+    ptx::mbar_block_sync(endbar);
     if (warp == 1) {
         __syncwarp();
         ptx::tc_fence_after();

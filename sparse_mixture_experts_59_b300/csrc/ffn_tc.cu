@@ -55,7 +55,7 @@ constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, MMA_N);
 constexpr int OFF_A = 0;
 constexpr int OFF_B = STAGES * A_BYTES;
 constexpr int OFF_BAR = OFF_B + STAGES * B_BYTES;
-constexpr int NUM_BARS = 2 * STAGES + 2 + 2 + 1;
+constexpr int NUM_BARS = 2 * STAGES + 2 + 2 + 1 + 1;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;          // tmem base, abort flag
 constexpr int OFF_START = OFF_MISC + 16;                  // group tile starts
 constexpr int OFF_OFFS = OFF_START + (kMaxExperts + 2) * 4;  // cached offsets
@@ -80,6 +80,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
     uint64_t* tfull = bars + 2 * STAGES;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
+    uint64_t* endbar = drain + 1;            // teardown: every thread
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
     volatile int* s_abort = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
     int* s_start = reinterpret_cast<int*>(smem + OFF_START);
@@ -97,6 +98,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
             ptx::mbar_init(&tempty[a], 128);
         }
         ptx::mbar_init(drain, 1);
+        ptx::mbar_init(endbar, NUM_THREADS);
         *s_abort = 0;
         ptx::fence_mbarrier_init();
         ptx::prefetch_tensormap(&mapA);
@@ -213,10 +215,9 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
         }
     }
 
-    // teardown: all roles done (or aborted; block_sync reconverges the warps
-    // whose lane 0 ran a role loop); free TMEM
+    // teardown: all roles done (or aborted); free TMEM
     ptx::tc_fence_before();
-    block_sync();
+    ptx::mbar_block_sync(endbar);
     if (warp == 1) {
         __syncwarp();
         ptx::tc_fence_after();

@@ -56,6 +56,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
     }
 }
 
+// Block-wide barrier of a kernel's teardown, on an mbarrier initialised with
+// the block's thread count: every thread arrives once and waits for the phase.
+// (Measured in the low-bit expert GEMM: a bar.sync after the role loops let
+// warps through before the epilogue warps had arrived, so tensor memory was
+// freed while the epilogue still read it.)  Bounded like mbar_wait.
+__device__ __forceinline__ void mbar_block_sync(uint64_t* bar) {
+    mbar_arrive(bar);
+    mbar_wait(bar, 0, nullptr);
+}
+
 // ----------------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
