@@ -45,7 +45,7 @@ def kernels_per_step(cfg):
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="mixtral_prefill")
@@ -380,6 +380,23 @@ def weight_bytes(cfg, counts_kept):
     return hit * per + 3 * d * Fs * (4 if cfg["dtype"] == "f32" else 2), hit
 
 
+def pick_tensor_peak(burst, sustained, region_ms, clk):
+    """The bf16 tensor peak a timed pass is judged against: the burst figure
+    for a pass of up to 100 ms at full clock, the sustained (power-capped)
+    figure for a longer pass or one whose median SM clock sat below 90% of the
+    maximum.  Returns (peak, name, reason)."""
+    mhz = clk.get("sm_mhz") if clk else None
+    mx = clk.get("sm_max_mhz") if clk else None
+    if region_ms > 100.0:
+        return sustained, "bf16_tflops_sustained", "the timed region is %.0f ms of back-to-back " \
+            "layer calls" % region_ms
+    if mhz and mx and mhz < 0.9 * mx:
+        return sustained, "bf16_tflops_sustained", "median SM clock %.0f of %.0f MHz in the " \
+            "timed region" % (mhz, mx)
+    return burst, "bf16_tflops", "burst: the timed region is %.0f ms at a median %s MHz" % (
+        region_ms, "%.0f" % mhz if mhz else "unknown")
+
+
 def gemm_roofline(alg, wbytes, gemm_s, peaks):
     """The grouped GEMMs' roofline time max(flop / tensor peak, weight bytes /
     HBM peak) at the burst tensor peak (the GEMMs are timed over tens of
@@ -418,21 +435,23 @@ def run_ours(args, world, rank, local):
 
     up_s = stages["up_gemm"] / 1e3
     dn_s = stages["down_gemm"] / 1e3
-    # the timed region lasts tens of milliseconds: the burst peak applies
     burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    sustained = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    peak, peak_kind, peak_why = pick_tensor_peak(burst, sustained, ms * args.steps, clk)
     up_tf = alg["up"] / up_s / 1e12
     kname = "up_gemm/%s" % (args.gemm or "auto")
     traffic, digest = recorded_traffic(args.workload, kname) if args.tokens is None and \
         args.experts is None else (None, None)
     mhz = clk.get("sm_mhz") if clk else None      # absent when no sample fell inside the passes
     roof = {"kernel": "up-projection grouped GEMM (SwiGLU epilogue)", "bound": "tensor",
-            "achieved": round(up_tf, 1), "peak": burst, "unit": "TFLOP/s",
-            "frac": round(up_tf / burst, 4), "traffic": traffic,
+            "achieved": round(up_tf, 1), "peak": peak, "unit": "TFLOP/s",
+            "frac": round(up_tf / peak, 4), "traffic": traffic,
+            "frac_of_burst_peak": round(up_tf / burst, 4),
+            "frac_of_sustained_peak": round(up_tf / sustained, 4),
             "traffic_note": "ncu dram__bytes_read.sum + dram__bytes_write.sum per launch, "
                             "profiles/traffic_%s.txt; null if the kernel sources changed "
                             "since (sources digest %s)" % (args.workload, digest),
-            "peak_source": "%s bf16_tflops (burst: the timed region is %d layer calls, "
-                           "%.0f ms)" % (peak_src, args.steps, ms * args.steps),
+            "peak_source": "%s %s (%s)" % (peak_src, peak_kind, peak_why),
             "algorithmic_flop_per_launch": alg["up"], "launch_ms": round(stages["up_gemm"], 4),
             "launch_mcycles_at_median_sm_clock": round(stages["up_gemm"] * mhz / 1e3, 4)
             if mhz else None}
@@ -454,8 +473,8 @@ def run_ours(args, world, rank, local):
                    "parallelism": "replicas" if world > 1 else "single",
                    "gemm_kernel": args.gemm or "auto"},
         "roofline": roof,
-        "grouped_gemm": {"tflops": round(gg_tf, 1), "frac_of_peak": round(gg_tf / burst, 4),
-                         "peak": burst, "up_ms": round(stages["up_gemm"], 4),
+        "grouped_gemm": {"tflops": round(gg_tf, 1), "frac_of_peak": round(gg_tf / peak, 4),
+                         "peak": peak, "up_ms": round(stages["up_gemm"], 4),
                          "down_ms": round(stages["down_gemm"], 4),
                          "down_tflops": round(alg["down"] / dn_s / 1e12, 1),
                          "roofline": gemm_roofline(alg, wbytes, up_s + dn_s, peaks)},

@@ -44,7 +44,8 @@ router_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constan
     uint64_t* full = bars;
     uint64_t* empty = bars + STAGES;
     uint64_t* done = bars + 2 * STAGES;
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(done + 1);
+    uint64_t* endbar = done + 1;              // teardown: every thread
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(endbar + 1);
     volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -60,6 +61,7 @@ router_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constan
             ptx::mbar_init(&empty[s], 1);
         }
         ptx::mbar_init(done, 1);
+        ptx::mbar_init(endbar, blockDim.x);
         *s_abort = 0;
         ptx::fence_mbarrier_init();
     }
@@ -146,7 +148,7 @@ router_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constan
         if (lane == 0) raise_error(status, MOE_ERR_DEVICE_TIMEOUT);
     }
     ptx::tc_fence_before();
-    block_sync();
+    ptx::mbar_block_sync(endbar);      // every warp's TMEM loads done, then free it
     if (warp == 1) {
         __syncwarp();
         ptx::tc_fence_after();
@@ -169,7 +171,7 @@ RouterPlan router_tc_plan(int T, int d, int E) {
     if (splits < 1) splits = 1;
     p.kb_per_split = (p.nkb + splits - 1) / splits;
     p.splits = (p.nkb + p.kb_per_split - 1) / p.kb_per_split;
-    p.smem = STAGES * (A_BYTES + b_stage_bytes(p.NB)) + (2 * STAGES + 1) * 8 + 16 + 1024;
+    p.smem = STAGES * (A_BYTES + b_stage_bytes(p.NB)) + (2 * STAGES + 2) * 8 + 16 + 1024;
     return p;
 }
 

@@ -93,3 +93,16 @@ def test_gemm_roofline_takes_the_slower_roof():
     assert r["frac"] == pytest.approx(0.75)
     r = bench.gemm_roofline(alg, 25e9, 10e-3, peaks)       # 5 ms of bytes
     assert r["bound"] == "hbm" and r["frac"] == pytest.approx(0.5)
+
+
+def test_tensor_peak_follows_the_timed_region():
+    """A short pass at full clock is judged against the burst peak; a long pass,
+    or one whose clock sat well below its maximum (the power cap), against the
+    sustained peak."""
+    full = {"sm_mhz": 2032.0, "sm_max_mhz": 2032.0}
+    capped = {"sm_mhz": 1342.0, "sm_max_mhz": 2032.0}
+    assert bench.pick_tensor_peak(1772.9, 1366.0, 40.0, full)[0] == 1772.9
+    assert bench.pick_tensor_peak(1772.9, 1366.0, 497.0, full)[0] == 1366.0
+    assert bench.pick_tensor_peak(1772.9, 1366.0, 40.0, capped)[0] == 1366.0
+    assert bench.pick_tensor_peak(1772.9, 1366.0, 40.0, None)[0] == 1772.9
+    assert bench.pick_tensor_peak(1772.9, 1366.0, 40.0, {"error": "no samples"})[0] == 1772.9
