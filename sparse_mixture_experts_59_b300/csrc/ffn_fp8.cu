@@ -29,22 +29,23 @@
 // MMA read), which at 128 B/clock caps the weight stream near the HBM rate;
 // through TMEM it is 2 bytes.
 //
-// One CTA per SM, 512 threads; the warps that issue TMA or MMA instructions
+// One CTA per SM, 384 threads for E4M3 and 512 for E2M1; the warps that issue TMA or MMA instructions
 // sit on different schedulers (warp % 4), as issuing them slows the other
 // warps of the scheduler (measured: a converter warp sharing its scheduler
 // with two MMA issuers ran ~2400 clocks behind one sharing with none, and the
 // slowest converter gates both the weight ring and the MMAs):
 //   warp 0      TMA: weight rows (E4M3: 128 bytes of K, 128-byte swizzle;
-//               E2M1: 80 bytes) into a ring of stages of two blocks, 160 KB
-//               in all, that the converters release as soon as they hold a
+//               E2M1: 80 bytes) into rings of stages (one ring per converter
+//               set, 160 KB in all; a stage is one E4M3 block or two E2M1
+//               blocks) that the converters release as soon as they hold a
 //               stage's codes in registers;
 //   warp 1      TMEM owner; TMA: the tile's f16 token rows (128-byte swizzle)
 //               in chunks of up to 24 KB into two buffers, a chunk ahead;
-//   warps 6-13  converters, two sets of one warp per TMEM lane quadrant; set
-//               z takes stage z of each k-block (blocks 2z, 2z + 1), thread
-//               = weight row: codes -> f16 pairs in registers, tcgen05.st
-//               into the TMEM A buffer of each block;
-//   last two    MMA issuers, issuer i for the blocks set i fills:
+//   warps 6..   converters, one set (E4M3) or two (E2M1) of one warp per
+//               TMEM lane quadrant; set z takes the stages of its blocks from
+//               a ring of its own, thread = weight row: codes -> f16 pairs in
+//               registers, tcgen05.st into the TMEM A buffer of each block;
+//   last two    MMA issuers, issuer i for blocks 2i and 2i + 1:
 //               tcgen05.mma kind::f16 (M=128, N=tokens, K=16), A from the
 //               block's TMEM buffer, B (tokens) from shared memory, into the
 //               block's accumulator.  A thread issues a small MMA only every
@@ -115,25 +116,29 @@ constexpr int XCH_LD = 33;
 // stream's pace (measured: a bare TMA ring of 10 KB stages streams 5.2 TB/s,
 // of 20 KB stages 6.6 TB/s, at the same 160 KB in flight).
 //
-// The converters are two sets of four warps; set z converts blocks BPS z ..
-// BPS z + BPS - 1 of every k-block, which MMA issuers BPS z .. consume.  Each set
-// has a ring of its own (RS slots): a slot shared by two consumers that run
-// at their own pace could see its barrier two phases ahead of one of them,
-// where a parity wait cannot tell the phases apart.
+// The converters are SETS sets of four warps; set z converts blocks BPS z ..
+// BPS z + BPS - 1 of every k-block.  Each set has a ring of its own (RS
+// slots): a slot shared by two consumers that run at their own pace could see
+// its barrier two phases ahead of one of them, where a parity wait cannot
+// tell the phases apart.  Packed E2M1 has two sets (a block's conversion
+// costs twice E4M3's: a cvt and a block-scale multiply per code pair); E4M3
+// has one (measured: a second set made its stream-bound up-projection ~5%
+// slower).
 enum { kFmtE4M3 = 0, kFmtE2M1 = 1 };
-constexpr int BPS = G / 2;                     // blocks per converter set
 constexpr int BPI = G / NISS;                  // blocks per MMA issuer
-static_assert(G % 2 == 0 && G % NISS == 0 && BPS % BPI == 0, "two converter sets; issuers within a set");
+static_assert(G % NISS == 0, "whole blocks per issuer");
 template <int FMT>
 struct WF {
     static constexpr int ROW_BYTES = FMT == kFmtE4M3 ? 128 : 80;
     static constexpr int SB = FMT == kFmtE4M3 ? 1 : 2;          // blocks per ring stage
     static constexpr int BLK_BYTES = WROWS * ROW_BYTES;         // one block of a k-block
     static constexpr int WQ_BYTES = SB * BLK_BYTES;             // one ring stage
-    static constexpr int RS = FMT == kFmtE4M3 ? 5 : 4;          // slots per set: 160 KB in flight
-    static constexpr int WSTAGES = 2 * RS;
-    static constexpr int CVT_WARPS = 8;                         // two sets of four, one warp per lane quadrant
-    static_assert(BPS % SB == 0, "a set's blocks are whole stages");
+    static constexpr int SETS = FMT == kFmtE4M3 ? 1 : 2;        // converter sets
+    static constexpr int BPS = G / SETS;                        // blocks per converter set
+    static constexpr int RS = FMT == kFmtE4M3 ? 10 : 4;         // slots per set: 160 KB in flight
+    static constexpr int WSTAGES = SETS * RS;
+    static constexpr int CVT_WARPS = 4 * SETS;                  // one warp per lane quadrant and set
+    static_assert(G % SETS == 0 && BPS % SB == 0, "a set's blocks are whole stages");
     static constexpr int MMA_WARP0 = 6 + CVT_WARPS;             // first MMA issuer
     static constexpr int NUM_THREADS = (MMA_WARP0 + NISS) * 32;
     static constexpr int OFF_TOK = 0;
@@ -155,7 +160,7 @@ struct WF {
                   "swizzled weight stages");
     static_assert(BLK_BYTES % 1024 == 0 || FMT != kFmtE4M3, "swizzled second box");
     static_assert(BLK_BYTES % 256 == 0, "128-byte aligned weight boxes");
-    static_assert(CVT_WARPS == 8, "two converter sets");
+    static_assert(SETS <= 2, "ring bookkeeping for up to two sets");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 template struct WF<kFmtE4M3>;
@@ -461,7 +466,7 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
                 for (int kb = t.kb0; ok && kb < t.kb1; ++kb)
                     for (int st = 0; st < nst; ++st, ++it) {
                         if (it == hold_it) { ok = false; held = true; break; }   // test hook
-                        const int z = st * F::SB / BPS, u = z ? used1++ : used0++;
+                        const int z = st * F::SB / F::BPS, u = z ? used1++ : used0++;
                         const int s = z * F::RS + u % F::RS;
                         const uint32_t ph = (uint32_t)(u / F::RS) & 1u;
                         if (!ptx::mbar_wait_nap(&wempty[s], ph ^ 1u, s_abort, 64)) { ok = false; break; }
@@ -477,7 +482,7 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
                 *s_abort = 1;
                 raise_error(p.status, MOE_ERR_DEVICE_TIMEOUT);
             }
-            for (int z = 0; z < 2; ++z) {        // the copies still in flight
+            for (int z = 0; z < F::SETS; ++z) {  // the copies still in flight
                 const int n = z ? used1 : used0;
                 for (int j = (n > F::RS ? n - F::RS : 0); j < n; ++j)
                     ptx::mbar_wait(&wfull[z * F::RS + j % F::RS], (uint32_t)(j / F::RS) & 1u, nullptr);
@@ -620,7 +625,7 @@ ffn_fp8_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
         FOR_EACH_SEG(t)
             const int nst = (t.nblk + SB - 1) / SB;
             for (int kb = t.kb0; ok && kb < t.kb1; ++kb)
-                for (int st = z * BPS / SB; ok && st < min(nst, (z + 1) * BPS / SB); ++st, ++u) {
+                for (int st = z * F::BPS / SB; ok && st < min(nst, (z + 1) * F::BPS / SB); ++st, ++u) {
                     const int s = z * F::RS + u % F::RS;
                     const uint32_t ph = (uint32_t)(u / F::RS) & 1u;
                     if (!__all_sync(0xffffffffu, ptx::mbar_wait(&wfull[s], ph, s_abort))) {
