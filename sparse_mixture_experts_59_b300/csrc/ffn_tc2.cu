@@ -218,7 +218,13 @@ ffn_tc2_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
     // teardown: both CTAs finished (no remote arrive still targets either),
     // then each frees its half of the pair's TMEM allocation
     ptx::tc_fence_before();
-    block_sync();
+    // The cluster barrier is what holds every warp here: the lanes of a role
+    // warp reach this point apart, so the block barrier may count such a warp
+    // early; the __syncwarp reconverges it before the (aligned) cluster
+    // barrier.  Reconverging before the block barrier instead measured 1-2%
+    // slower on the grouped GEMMs of the prefill layer.
+    __syncthreads();
+    __syncwarp();
     ptx::cluster_sync();
     if (warp == 1) {
         __syncwarp();
