@@ -163,15 +163,24 @@ RouterPlan router_tc_plan(int T, int d, int E) {
     p.NB = (E + 15) / 16 * 16;
     p.m_tiles = (T + BM - 1) / BM;
     p.nkb = (d + BK - 1) / BK;
+    p.smem = STAGES * (A_BYTES + b_stage_bytes(p.NB)) + (2 * STAGES + 2) * 8 + 16 + 1024;
     // about two CTAs per SM stream x at once; few tokens (one or two M tiles)
     // take at most 16 splits, as the top-k kernel adds the partials per token
     const int target = p.m_tiles <= 2 ? 16 * p.m_tiles : 2 * 148;
     int splits = (target + p.m_tiles - 1) / p.m_tiles;
+    // A grid larger than the CTAs the 148 SMs hold at once (228 KB of shared
+    // memory per SM with 1 KB reserved per CTA, 512 tensor-memory columns)
+    // ends in a partial wave that streams x at a fraction of the bandwidth;
+    // fewer, longer splits keep it to one wave.
+    const int by_smem = (228 * 1024) / (p.smem + 1024);
+    const int by_tmem = 512 / tmem_cols_for(p.NB);
+    const int per_sm = by_smem < by_tmem ? by_smem : by_tmem;
+    const int resident = 148 * (per_sm > 1 ? per_sm : 1);
+    if (p.m_tiles * splits > resident) splits = resident / p.m_tiles;
     if (splits > p.nkb) splits = p.nkb;
     if (splits < 1) splits = 1;
     p.kb_per_split = (p.nkb + splits - 1) / splits;
     p.splits = (p.nkb + p.kb_per_split - 1) / p.kb_per_split;
-    p.smem = STAGES * (A_BYTES + b_stage_bytes(p.NB)) + (2 * STAGES + 2) * 8 + 16 + 1024;
     return p;
 }
 
