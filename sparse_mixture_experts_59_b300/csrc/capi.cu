@@ -32,8 +32,10 @@ size_t esize(const moe_cfg& c) { return c.dtype == MOE_F32 ? 4 : 2; }
 size_t align_up(size_t v) { return (v + 255) & ~(size_t)255; }
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-constexpr int kRouterTopkMaxBlocks = 1024;  // one token per warp up to T = 8192; P partials
-                                            // of the blocks are added at the end
+// The top-k kernel's 256-thread blocks take 64 registers a thread, so an SM
+// holds 4: 592 blocks are one wave.  More would only add a partial wave and
+// rows to the P partials that the last block adds up alone.
+constexpr int kRouterTopkMaxBlocks = 4 * 148;
 int router_blocks(int T) {
     const int b = (T + 7) / 8;
     return b < 1 ? 1 : (b > kRouterTopkMaxBlocks ? kRouterTopkMaxBlocks : b);

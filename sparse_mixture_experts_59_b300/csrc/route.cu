@@ -152,7 +152,7 @@ router_topk_kernel(const float* part, int nsplit, const float* __restrict__ bias
     __threadfence();
     // column sums of prob_part[nblocks][E], in a fixed order so that the
     // result repeats exactly.  One block reads all nblocks x E partials (up to
-    // 1024 x 256), so the loads go 16 bytes and 8 at a time: with E a multiple
+    // 592 x 256), so the loads go 16 bytes and 8 at a time: with E a multiple
     // of 4, thread t adds rows g, g+G, ... (g = t / C, G = 256 / C groups) of
     // the 4 experts of float4 column t % C (C = E / 4), then the groups are
     // added in order; otherwise one expert per thread the same way.
