@@ -106,3 +106,22 @@ def test_tensor_peak_follows_the_timed_region():
     assert bench.pick_tensor_peak(1772.9, 1366.0, 40.0, capped)[0] == 1366.0
     assert bench.pick_tensor_peak(1772.9, 1366.0, 40.0, None)[0] == 1772.9
     assert bench.pick_tensor_peak(1772.9, 1366.0, 40.0, {"error": "no samples"})[0] == 1772.9
+
+
+def test_recorded_traffic_needs_the_digest_it_was_taken_on(tmp_path, monkeypatch):
+    """The DRAM-traffic figure in a profile is reported only while the GEMM
+    kernel sources hash to the digest recorded beside it. After an edit the
+    figure is withheld (None), and so is one for a kernel the file does not
+    list."""
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "traffic_demo.txt").write_text(
+        "# header line\ntraffic up_gemm/swap 123456 abcdef0123456789\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_sources_digest", lambda: "abcdef0123456789")
+    assert bench.recorded_traffic("demo", "up_gemm/swap") == (123456, "abcdef0123456789")
+    assert bench.recorded_traffic("demo", "up_gemm/tc1")[0] is None
+    assert bench.recorded_traffic("other", "up_gemm/swap") == (None, None)
+    monkeypatch.setattr(bench, "kernel_sources_digest", lambda: "0000000000000000")
+    assert bench.recorded_traffic("demo", "up_gemm/swap") == (None, "0000000000000000")
+
