@@ -343,6 +343,30 @@ def test_page_example_shapes_and_parameter_counts():
     assert abs(m["E"] * per_expert - float(g["mixtral.layer_ffn_params.approx"])) / 1.41e9 < 0.005
 
 
+
+def test_mixtral_shape_against_the_pages_parameter_totals():
+    """The pages give Mixtral 8x7B as 46.7B parameters held and 12.9B active
+    per token. Attention, embeddings and norms count in both totals, so the
+    difference is the (E - k) unused expert FFNs of every layer:
+    layers x (E - k) x 3 d F, with each total rounded to 0.1B. The layer-wise
+    breakdown (32 x (8 experts + ~67M attention) ~ 47B; 32 x (2 experts +
+    attention) ~ 13B) must also hold for the Mixtral workload's d, F, E and k.
+    A wrong k, E, d or F misses the difference by whole billions."""
+    g = _golden("mixtral_param_counts.txt")
+    m = workloads.config("mixtral_prefill")
+    layers = int(g["mixtral.layers"])
+    per_expert = 3 * m["d"] * m["F"]
+    idle = layers * (m["E"] - m["k"]) * per_expert
+    printed = float(g["mixtral.total_params"]) - float(g["mixtral.active_params"])
+    assert abs(idle - printed) <= 0.1e9
+    attn = float(g["mixtral.attention_params_per_layer.approx"])
+    total = layers * (m["E"] * per_expert + attn)
+    active = layers * (m["k"] * per_expert + attn)
+    assert abs(total - float(g["mixtral.total_params_layerwise.approx"])) / 47e9 < 0.01
+    assert abs(active - float(g["mixtral.active_params_layerwise.approx"])) / 13e9 < 0.05
+    # the decode workload streams the same weights
+    assert workloads.config("mixtral_decode")["E"] == m["E"]
+
 def test_workload_capacities_and_skew():
     """The tiny workload has capacity 20 and the skewed Switch workload 256;
     the skew offsets fall with expert index as -1.8 ln(e+1)."""
