@@ -153,3 +153,17 @@ def test_config_kernel_choice_fields_are_validated(lib):
     c.route_path = 2
     assert lib.moe_workspace_size(ctypes.byref(c), ctypes.byref(n)) == 1
     assert "route_path" in lib.moe_last_error().decode()
+
+
+def test_a_missing_library_fails_loudly(tmp_path, monkeypatch):
+    """Without the built CUDA library the binding raises on the first call
+    that needs it. No stage has a CPU path to fall back to."""
+    monkeypatch.setattr(binding, "LIB_PATH", str(tmp_path / "libmoe_b300.so"))
+    monkeypatch.setattr(binding, "_lib", None)
+    with pytest.raises(RuntimeError, match="not found"):
+        binding.lib()
+    cfg = workloads.config("tiny_fp32")
+    with pytest.raises(RuntimeError, match="not found"):
+        binding.capacity(binding.make_config(cfg))
+    with pytest.raises(RuntimeError, match="not found"):
+        binding.workspace_size(binding.make_config(cfg))
