@@ -34,7 +34,8 @@
  *  - "Assignment" a = t*k + s is slot s of token t.
  *  - dtype MOE_BF16: x, weights, biases, y and the slot buffer are bf16, router
  *    logits / weights fp32, accumulation fp32.  MOE_F32: everything fp32.
- *    bf16 buffers must be 16-byte aligned; d, F and F_shared multiples of 8.
+ *    bf16 buffers must be 16-byte aligned; d, F and F_shared multiples of 8;
+ *    E * max(d, F) below 2^31 (weight rows take 32-bit coordinates).
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *    default stream).  Host-side argument errors are returned before anything
  *    is launched.  Errors found on the device (an expert index out of range, a

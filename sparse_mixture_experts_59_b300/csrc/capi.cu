@@ -99,6 +99,10 @@ int check_cfg(const moe_cfg* c) {
     if ((long long)c->T * c->k > (1LL << 26)) return fail(MOE_ERR_INVALID_ARG, "T*k above 2^26%s");
     if (c->F_shared < 0 || c->F_shared % 8)
         return fail(MOE_ERR_INVALID_ARG, "F_shared must be 0 or a multiple of 8%s");
+    // the expert GEMMs address weight rows (expert x outputs) with 32-bit
+    // coordinates, in the kernels and in the TMA maps
+    if ((long long)c->E * (c->F > c->d ? c->F : c->d) >= (1LL << 31))
+        return fail(MOE_ERR_INVALID_ARG, "E*max(d, F) must stay below 2^31%s");
     if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return fail(MOE_ERR_INVALID_ARG, "unknown dtype%s");
     if (c->act != MOE_GELU_ERF && c->act != MOE_SWIGLU) return fail(MOE_ERR_INVALID_ARG, "unknown act%s");
     if (c->has_bias && c->act == MOE_SWIGLU)

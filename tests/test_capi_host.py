@@ -63,6 +63,8 @@ def test_workspace_size_grows_with_tokens(lib):
     (dict(d=12), 1), (dict(F=0), 1), (dict(E=0), 1), (dict(E=300), 1), (dict(k=0), 1),
     (dict(k=9, E=16), 1), (dict(k=3, E=2), 1), (dict(T=-1), 1), (dict(F_shared=4), 1),
     (dict(act="swiglu", has_bias=True), 2), (dict(act="gelu", F_shared=64), 2),
+    # weight rows past 32-bit coordinates
+    (dict(E=256, F=1 << 23), 1), (dict(E=2, k=2, d=1 << 30), 1),
     # packed 4-bit weights: 128-value chunks, not with FP8 or an fp32 layer
     (dict(weight_fp4=True), 1), (dict(weight_fp4=True, d=128, F=192), 1),
     (dict(weight_fp4=True, weight_fp8=True, d=128, F=128), 1),
