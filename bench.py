@@ -380,6 +380,26 @@ def weight_bytes(cfg, counts_kept):
     return hit * per + 3 * d * Fs * (4 if cfg["dtype"] == "f32" else 2), hit
 
 
+REJECT_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
+
+
+def clock_rejection(clk, low_frac=0.85):
+    """Why a timed pass's clock record disqualifies its number, or None.
+    Two things disqualify it: a hardware or thermal slowdown seen during the
+    pass, or a median SM clock well below the maximum with no reason reported
+    (a clock lock left by an earlier user). The power cap alone is kept,
+    since it is the normal state of a long dense run."""
+    if not clk or "sm_mhz" not in clk:
+        return None
+    bad = [r for r in clk.get("reasons", []) if r in REJECT_REASONS]
+    if bad:
+        return "clock-event reasons during the pass: " + ", ".join(bad)
+    mx = clk.get("sm_max_mhz")
+    if mx and clk["sm_mhz"] < low_frac * mx and not clk.get("reasons"):
+        return "median SM clock %.0f of %.0f MHz with no reason reported" % (clk["sm_mhz"], mx)
+    return None
+
+
 def pick_tensor_peak(burst, sustained, region_ms, clk):
     """The bf16 tensor peak a timed pass is judged against: the burst figure
     for a pass of up to 100 ms at full clock, the sustained (power-capped)
@@ -428,6 +448,17 @@ def run_ours(args, world, rank, local):
                                                                    device=dev)}
     clocks = ClockSampler(local)
     ms_local, stages, clk = time_layer(layer, x, args.steps, args.warmup, world, outputs, clocks)
+    # a pass whose clock record disqualifies it is taken once more after a
+    # longer idle; every rank takes part when any rank's record asks for it
+    why = clock_rejection(clk)
+    remeasured = None
+    if max_over_ranks(1.0 if why else 0.0, world) > 0:
+        remeasured = {"first_ms_per_step": round(ms_local, 4), "first_clocks": clk,
+                      "why": why or "another rank's clock record"}
+        time.sleep(5.0)
+        clocks = ClockSampler(local)
+        ms_local, stages, clk = time_layer(layer, x, args.steps, args.warmup, world, outputs,
+                                           clocks)
     ms = max_over_ranks(ms_local, world)
     R = int(outputs["counts_kept"].sum().item())
     alg = algorithmic(cfg, R)
@@ -485,6 +516,7 @@ def run_ours(args, world, rank, local):
         "gpu_launches": kernels_per_step(cfg) * args.steps,
         "pdl": os.environ.get("MOE_PDL", "1") != "0",
         "clocks": clk,
+        **({"remeasured": remeasured} if remeasured else {}),
     }
     if args.sustained_seconds > 0:
         result["sustained"] = run_sustained(layer, x, outputs, cfg, alg, args, world, peaks,

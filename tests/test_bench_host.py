@@ -125,3 +125,21 @@ def test_recorded_traffic_needs_the_digest_it_was_taken_on(tmp_path, monkeypatch
     monkeypatch.setattr(bench, "kernel_sources_digest", lambda: "0000000000000000")
     assert bench.recorded_traffic("demo", "up_gemm/swap") == (None, "0000000000000000")
 
+
+
+def test_clock_records_that_disqualify_a_pass():
+    """A hardware or thermal slowdown, or a clock held well below its maximum
+    with no reason given, sends the pass to be taken again. The power cap
+    alone, a full clock, or a record with no samples does not."""
+    ok = {"sm_mhz": 2032.0, "sm_max_mhz": 2032.0, "reasons": []}
+    capped = {"sm_mhz": 1320.0, "sm_max_mhz": 2032.0, "reasons": ["sw_power_cap"]}
+    assert bench.clock_rejection(ok) is None
+    assert bench.clock_rejection(capped) is None
+    assert bench.clock_rejection(None) is None
+    assert bench.clock_rejection({"error": "no samples"}) is None
+    for r in ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"):
+        why = bench.clock_rejection(dict(ok, reasons=["sw_power_cap", r]))
+        assert why is not None and r in why
+    locked = {"sm_mhz": 1400.0, "sm_max_mhz": 2032.0, "reasons": []}
+    assert "no reason" in bench.clock_rejection(locked)
+    assert bench.clock_rejection(dict(locked, sm_mhz=1900.0)) is None
